@@ -1,0 +1,164 @@
+"""Seeded synthetic decode-attention inputs.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic.  Both the CUDA path's tests/bench and the CPU oracle take
+their inputs from here, so the two sides see bit-identical bf16 tensors.
+
+Layout (the ragged "packed" KV cache used throughout the library):
+  q          bf16 [B, Hq, D]
+  k, v       bf16 [T, Hkv, D]     T = kv_indptr[B]; request b owns rows
+                                   kv_indptr[b] .. kv_indptr[b+1]-1
+  kv_indptr  int32 [B+1]          kv_indptr[0] = 0, non-decreasing
+  scale      Python float holding an fp32 value (1/sqrt(D) rounded to fp32)
+
+Recipe (one torch CPU generator per workload, seed = 42 + index, draws in this
+order; every draw is fp32 and then rounded to bf16 with round-to-nearest-even):
+  1. per-request lengths (ragged workload only): integers uniform in [lo, hi]
+  2. q
+  3. K  (drawn in blocks of 65536 tokens, in token order)
+  4. outlier positions (stressed workload only): for each (request b, kv head h)
+     round(0.001 * L_b) distinct token positions, taken from a seeded
+     permutation; K[pos, h, :] *= 16 before the bf16 rounding
+  5. V  (same blocking as K)
+The seed base 42 is the seed of the equivalence check printed on the
+FlashDecoding++ sequence-split article (techknowgenie.com), section 5.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+_BLOCK_TOKENS = 65536
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic decode workload: shapes plus value distributions."""
+    name: str
+    index: int
+    batch: int
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    kv_len: int | None            # fixed length, or None when ragged
+    ragged: tuple | None = None   # (lo, hi) inclusive, when ragged
+    q_std: float = 1.0
+    v_dist: str = "normal"        # "normal" (N(0,1)) or "uniform" (U(-1,1))
+    k_outlier_frac: float = 0.0   # fraction of positions per (request, head) scaled
+    k_outlier_mult: float = 16.0
+    description: str = field(default="", compare=False)
+
+
+# The five decode workloads the benchmark and the full-size parity tests use.
+WORKLOADS = [
+    Workload("tiny_mha_b1_h8_l2048", 0, 1, 8, 8, 128, 2048,
+             description="tiny MHA decode, B=1, Hq=Hkv=8, D=128, L=2048, N(0,1)"),
+    Workload("gqa_b1_h32x8_l65536", 1, 1, 32, 8, 128, 65536,
+             description="Llama-3-8B-shaped GQA decode, B=1, Hq=32, Hkv=8, L=65536, N(0,1)"),
+    Workload("gqa_b1_h32x8_l131072", 2, 1, 32, 8, 128, 131072,
+             description="GQA decode at 128k context, B=1, Hq=32, Hkv=8, L=131072, N(0,1)"),
+    Workload("ragged_b64_h32x8_l512to16384", 3, 64, 32, 8, 128, None, ragged=(512, 16384),
+             description="ragged batch, B=64, Hq=32, Hkv=8, L~U[512,16384], N(0,1)"),
+    Workload("stressed_b16_h64x8_l32768", 4, 16, 64, 8, 128, 32768,
+             q_std=2.0, v_dist="uniform", k_outlier_frac=0.001,
+             description="stressed GQA, B=16, Hq=64, Hkv=8, L=32768, K N(0,1) with 0.1% "
+                         "of positions per head x16, q std 2, V U(-1,1)"),
+]
+
+
+def workload(key) -> Workload:
+    """Look a workload up by index or by name."""
+    if isinstance(key, int):
+        return WORKLOADS[key]
+    for w in WORKLOADS:
+        if w.name == key:
+            return w
+    raise KeyError(key)
+
+
+def fp32_scale(head_dim: int) -> float:
+    """1/sqrt(D) rounded to fp32 (the same fp32 value is given to every side)."""
+    return float(np.float32(1.0 / math.sqrt(head_dim)))
+
+
+def _lengths(w: Workload, g: torch.Generator) -> list[int]:
+    if w.ragged is None:
+        return [w.kv_len] * w.batch
+    lo, hi = w.ragged
+    return torch.randint(lo, hi + 1, (w.batch,), generator=g, dtype=torch.int64).tolist()
+
+
+def _blocked_draw(shape_tail, rows, g, kind):
+    """Draw a [rows, *shape_tail] fp32 array block by block, return bf16."""
+    out = torch.empty((rows, *shape_tail), dtype=torch.bfloat16)
+    for r0 in range(0, rows, _BLOCK_TOKENS):
+        r1 = min(rows, r0 + _BLOCK_TOKENS)
+        if kind == "normal":
+            blk = torch.randn((r1 - r0, *shape_tail), generator=g, dtype=torch.float32)
+        else:
+            blk = torch.rand((r1 - r0, *shape_tail), generator=g, dtype=torch.float32) * 2.0 - 1.0
+        out[r0:r1] = blk.to(torch.bfloat16)
+    return out
+
+
+def make_inputs(key, *, seed: int | None = None) -> dict:
+    """Build one workload's inputs on the CPU (torch tensors, bf16 / int32)."""
+    w = workload(key)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(42 + w.index if seed is None else seed)
+    lengths = _lengths(w, g)
+    indptr = np.zeros(w.batch + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(lengths)
+    total = int(indptr[-1])
+    assert total < 2**31, "token count must fit int32"
+    D, Hq, Hkv = w.head_dim, w.num_qo_heads, w.num_kv_heads
+
+    q = (torch.randn((w.batch, Hq, D), generator=g, dtype=torch.float32) * w.q_std).to(torch.bfloat16)
+
+    if w.k_outlier_frac > 0.0:
+        # Draw K in fp32, apply the outlier multiplier, then round to bf16.
+        k32 = torch.empty((total, Hkv, D), dtype=torch.float32)
+        for r0 in range(0, total, _BLOCK_TOKENS):
+            r1 = min(total, r0 + _BLOCK_TOKENS)
+            k32[r0:r1] = torch.randn((r1 - r0, Hkv, D), generator=g, dtype=torch.float32)
+        for b in range(w.batch):
+            L = lengths[b]
+            n = int(round(w.k_outlier_frac * L))
+            for h in range(Hkv):
+                pos = torch.randperm(L, generator=g)[:n] + int(indptr[b])
+                k32[pos, h, :] *= w.k_outlier_mult
+        k = k32.to(torch.bfloat16)
+        del k32
+    else:
+        k = _blocked_draw((Hkv, D), total, g, "normal")
+
+    v = _blocked_draw((Hkv, D), total, g, w.v_dist)
+    return dict(
+        workload=w, q=q, k=k, v=v,
+        kv_indptr=torch.from_numpy(indptr.astype(np.int32)),
+        lengths=lengths, scale=fp32_scale(D),
+    )
+
+
+def make_small(batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+               lengths, *, seed: int = 0, q_std: float = 1.0, dtype=torch.bfloat16,
+               v_dist: str = "normal") -> dict:
+    """Small seeded inputs for parity and pin tests (same layout as make_inputs)."""
+    assert len(lengths) == batch
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    indptr = np.zeros(batch + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(lengths)
+    total = int(indptr[-1])
+    q = (torch.randn((batch, num_qo_heads, head_dim), generator=g) * q_std).to(dtype)
+    k = torch.randn((total, num_kv_heads, head_dim), generator=g).to(dtype)
+    if v_dist == "normal":
+        v = torch.randn((total, num_kv_heads, head_dim), generator=g).to(dtype)
+    else:
+        v = (torch.rand((total, num_kv_heads, head_dim), generator=g) * 2.0 - 1.0).to(dtype)
+    return dict(q=q, k=k, v=v, kv_indptr=torch.from_numpy(indptr.astype(np.int32)),
+                lengths=list(lengths), scale=fp32_scale(head_dim))
+
