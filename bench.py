@@ -1,0 +1,442 @@
+"""Benchmark of one split-KV decode-attention step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl fd|reference]
+
+A step is the whole path: the host plan (fd_plan), stage 1 (fd_decode_split)
+and stage 2 (fd_merge), through the C ABI, on one batch of seeded synthetic
+inputs already resident in HBM.  The default workload is the Llama-3-8B-shaped
+GQA decode at 64k context (B=1, Hq=32, Hkv=8, D=128, L=65536).  L2 is flushed
+(a 256 MiB write) between timed steps, outside the timed events.
+
+Prints one JSON line (rank 0).  `value` is achieved bandwidth in GB/s: the
+algorithmic bytes of a step (q + K + V + O + LSE + the partials written and
+read back) over the device time of the step; `ms_per_step` is that time.
+`--impl reference` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload, extrapolated to one step).
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (requests
+are independent, no collective on the data path); value = all ranks' bytes /
+the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, workload  # noqa: E402
+
+METRIC = "decode-attention µs/step and achieved HBM GB/s vs ~8 TB/s GB300 peak"
+DEFAULT_WORKLOAD = "gqa_b1_h32x8_l65536"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+SPLIT_SOURCES = ["split_kernel.cu", "device_common.cuh", "plan_rule.h", "fd_api.cu"]
+
+
+# ----------------------------------------------------------------- helpers
+
+def step_bytes(B, Hq, Hkv, D, T, rows) -> dict:
+    """Algorithmic bytes of one step and of each kernel launch."""
+    q = B * Hq * D * 2
+    kv = 2 * T * Hkv * D * 2
+    out = B * Hq * (D + 1) * 4
+    part = rows * (D + 1) * 4
+    return dict(step=q + kv + out + 2 * part, split=q + kv + part, merge=part + out,
+                kv=kv, q=q, out=out, partials=2 * part)
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def split_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in SPLIT_SOURCES:
+        with open(os.path.join(ROOT, "split_kv_flashdecoding_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per split-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != split_source_hash():
+        return None
+    entry = rec.get("workloads", {}).get(workload_name)
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed loop runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+        time.sleep(0.2)
+        return self
+
+    def mark(self):
+        self.t_start = time.time()
+
+    def __exit__(self, *exc):
+        self.t_end = time.time()
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+        self.file.flush()
+        self.file.close()
+
+    def summary(self) -> dict:
+        try:
+            lines = open(self.file.name).read().strip().splitlines()
+        except OSError:
+            lines = []
+        finally:
+            try:
+                os.unlink(self.file.name)
+            except OSError:
+                pass
+        samples = []
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        window = [s for s in samples if self.t_start - 0.05 <= s[0] <= self.t_end + 0.05] or samples
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in window for i, v in enumerate(s[3]) if v == "Active"})
+        return {"sm_mhz": float(np.median([s[1] for s in window])),
+                "sm_max_mhz": max(s[2] for s in window), "reasons": reasons,
+                "samples": len(window)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ fd arm
+
+def run_fd(args, world, rank, local) -> dict | None:
+    import torch
+
+    import split_kv_flashdecoding_gb300 as fd
+    from workloads import make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = workload(args.workload)
+    inp = make_inputs(w.index)
+    B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
+    ip_host = inp["kv_indptr"].numpy().astype(np.int32)
+    T = int(ip_host[-1])
+    q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
+    ip_dev = inp["kv_indptr"].to(dev)
+    scale = inp["scale"]
+
+    info0 = fd.plan(B, Hq, Hkv, D, ip_host)
+    rows = info0.num_partial_rows
+    nb = step_bytes(B, Hq, Hkv, D, T, rows)
+    ws = torch.zeros(fd.WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=dev)
+    po = torch.empty((rows, D), dtype=torch.float32, device=dev)
+    pl = torch.empty((rows,), dtype=torch.float32, device=dev)
+    o = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        info = fd.plan(B, Hq, Hkv, D, ip_host)             # host planner, every step
+        fd.decode_split(info, q, k, v, ip_dev, scale, po, pl, ws, stream=stream)
+        return info
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+        fd.merge(info0, ip_dev, po, pl, o, lse, ws, stream=stream)
+    torch.cuda.synchronize(dev)
+    if fd.get_device_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    launches = 0
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        clocks.mark()
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.fill_(float(i))                              # L2 flush, outside the events
+            ev[i][0].record(stream)
+            info = step()
+            ev[i][1].record(stream)
+            fd.merge(info, ip_dev, po, pl, o, lse, ws, stream=stream)
+            ev[i][2].record(stream)
+            launches += 2 if info.num_work > 0 else 1
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        barrier(world)
+    status = fd.get_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {fd.status_string(status)}")
+    step_ms = np.array([ev[i][0].elapsed_time(ev[i][2]) for i in range(K)])
+    split_ms = np.array([ev[i][0].elapsed_time(ev[i][1]) for i in range(K)])
+    merge_ms = np.array([ev[i][1].elapsed_time(ev[i][2]) for i in range(K)])
+    ms_local = float(step_ms.mean())
+    ms = max_over_ranks(ms_local, world, dev)
+    split_avg = float(split_ms.mean())
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, fd_decode, D2H of O and LSE, all inside the events
+    e2e = None
+    if not args.no_e2e:
+        q_h, k_h, v_h = (inp[x].pin_memory() for x in ("q", "k", "v"))
+        ip_h = inp["kv_indptr"].pin_memory()
+        o_h = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+        l_h = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+        wsd = torch.zeros(info0.workspace_bytes, dtype=torch.uint8, device=dev)
+        e2e_steps = max(3, min(K, 20))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(e2e_steps)]
+        for i in range(e2e_steps + 2):
+            flush.fill_(float(i))
+            if i >= 2:
+                evs[i - 2][0].record(stream)
+            q.copy_(q_h, non_blocking=True)
+            k.copy_(k_h, non_blocking=True)
+            v.copy_(v_h, non_blocking=True)
+            ip_dev.copy_(ip_h, non_blocking=True)
+            fd.decode(q, k, v, ip_host, ip_dev, scale, o=o, lse=lse, workspace=wsd, stream=stream)
+            o_h.copy_(o, non_blocking=True)
+            l_h.copy_(lse, non_blocking=True)
+            if i >= 2:
+                evs[i - 2][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evs])), world, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, ip_h))
+        d2h = sum(t.numel() * t.element_size() for t in (o_h, l_h))
+        e2e = {"value": round(world * nb["step"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peaks()
+    achieved = nb["split"] / (split_avg * 1e-3) / 1e9
+    traffic = profiled_traffic(w.name)
+    gbs = world * nb["step"] / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "us_per_step": round(ms * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 accumulate/out",
+        "data": "synthetic (seeded, see workloads/)",
+        "config": {"workload": w.name, "description": w.description, "batch": B,
+                   "num_qo_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "total_tokens": T,
+                   "chunk": info0.chunk, "splits": info0.total_splits, "ctas": info0.num_work,
+                   "ctas_per_sm": info0.ctas_per_sm, "num_sms": info0.num_sms,
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "algorithmic_bytes_per_step": nb["step"],
+                   "frac_of_nominal_8tbs": round(gbs / world / NOMINAL_HBM_GBS, 4),
+                   "split_us": round(split_avg * 1e3, 2),
+                   "merge_us": round(float(merge_ms.mean()) * 1e3, 2),
+                   "step_us_p10_p50_p90": [round(float(np.percentile(step_ms, p)) * 1e3, 2)
+                                           for p in (10, 50, 90)],
+                   "wall_s": round(t_wall, 3),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "split_kv_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "algorithmic_bytes_per_launch": nb["split"],
+                     "traffic": traffic},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, inp, nb["step"], budget_s=args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------- oracle (CPU) timing
+
+def _oracle_rows(inp, rows, threads) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"], rows=rows,
+                  threads=threads)
+    return time.perf_counter() - t0
+
+
+def _row_cost(w, inp, cores) -> float:
+    """Core-seconds of oracle work per (request, query head) row."""
+    rows = np.random.default_rng(1).permutation(w.batch * w.num_qo_heads)[:cores]
+    return _oracle_rows(inp, rows, cores) / len(rows) * cores
+
+
+def cpu_baseline(w, inp, step_bytes_total, budget_s=10.0) -> dict:
+    """Time the fp64 oracle on the host cores over a bounded sample of the
+    step's (request, query head) rows and extrapolate to one full step."""
+    cores = max(1, len(os.sched_getaffinity(0)))
+    all_rows = w.batch * w.num_qo_heads
+    per_row = _row_cost(w, inp, cores)
+    n = int(min(all_rows, max(min(cores, all_rows), budget_s * cores / max(per_row, 1e-9))))
+    rows = np.random.default_rng(0).permutation(all_rows)[:n]
+    t = _oracle_rows(inp, rows, cores)
+    step_s = t * all_rows / n
+    return {"value": round(step_bytes_total / step_s / 1e9, 4), "unit": "GB/s",
+            "us_per_step": round(step_s * 1e6, 1), "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {all_rows} (request, query-head) rows of {w.name}, "
+                      f"fp64 C oracle, {t:.2f} s wall on {cores} threads, "
+                      f"extrapolated to the full step"}
+
+
+def run_reference(args, world, rank) -> dict | None:
+    """The oracle arm: each timed step runs the fp64 oracle on a fixed sample
+    of the step's rows on the host cores (sized so the whole run takes about a
+    minute and a half) and is extrapolated to the full step."""
+    if rank != 0:
+        return None
+    import split_kv_flashdecoding_gb300 as fd   # host planner only: counts the partial bytes
+    from workloads import make_inputs
+    w = workload(args.workload)
+    inp = make_inputs(w.index)
+    B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
+    T = int(inp["kv_indptr"][-1])
+    rows_partial = fd.plan(B, Hq, Hkv, D, inp["kv_indptr"], num_sms=152).num_partial_rows
+    nb = step_bytes(B, Hq, Hkv, D, T, rows_partial)
+    cores = max(1, len(os.sched_getaffinity(0)))
+    all_rows = B * Hq
+    per_row = _row_cost(w, inp, cores)
+    per_step_budget = max(0.0, 90.0 / max(args.steps, 1))
+    n = int(min(all_rows, max(1, per_step_budget * cores / max(per_row, 1e-9))))
+    threads = min(cores, n)
+    sample = np.random.default_rng(0).permutation(all_rows)[:n]
+    for _ in range(args.warmup):
+        _oracle_rows(inp, sample[:1], 1)
+    times = [_oracle_rows(inp, sample, threads) for _ in range(args.steps)]
+    step_s = float(np.mean(times)) * all_rows / n
+    value = nb["step"] / step_s / 1e9
+    return {
+        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, see workloads/)",
+        "config": {"workload": w.name, "description": w.description},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{n} of {all_rows} (request, query-head) rows of {w.name} "
+                                   f"per step on {threads} threads, extrapolated to the full step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[x.name for x in WORKLOADS])
+    ap.add_argument("--impl", default="fd", choices=["fd", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle CPU work per timed sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_fd(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "fd":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * fd.h -- C ABI of libfd: split-KV ("flash-decoding") decode attention for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Method: "FlashDecoding++: sequence-dimension KV split parallelism for LLM
+ * serving" (techknowgenie.com).  §2 adds the sequence axis to the grid so a
+ * batch-1 decode step fills every SM; §3 computes a partial softmax per chunk
+ * (stage 1) and merges the partials by their log-sum-exp (stage 2); §6 (chunk
+ * size tuning guide) sizes the chunks from the SM count.
+ *
+ * What one decode step computes (for each request b and query head hq, with
+ * G = Hq / Hkv and KV head kvh = hq / G):
+ *     s_j   = scale * <q[b,hq,:], K[j,kvh,:]>      j in [kv_indptr[b], kv_indptr[b+1])
+ *     O     = sum_j softmax(s)_j * V[j,kvh,:]
+ *     LSE   = ln sum_j exp(s_j)
+ *
+ * Tensor layouts (all row-major, contiguous, device memory unless noted):
+ *     q          bf16  [B, Hq, D]
+ *     k, v       bf16  [T, Hkv, D]   ragged "packed" KV cache, T = kv_indptr[B]
+ *     kv_indptr  int32 [B+1]         0 = kv_indptr[0] <= ... <= kv_indptr[B] = T
+ *     o          fp32  [B, Hq, D]
+ *     lse        fp32  [B, Hq]       natural log; -inf for a request with no keys
+ *     partial_o  fp32  [num_partial_rows, D]
+ *     partial_lse fp32 [num_partial_rows]
+ * Partial row of (request b, query head hq, split s):
+ *     split_prefix[b] * Hq + hq * splits_b + s
+ * where splits_b is request b's split count and split_prefix[b] is the sum of
+ * splits_b' over b' < b.
+ *
+ * Supported: D = 128; G = Hq / Hkv in {1, 2, 4, 8}.  Others return
+ * FD_ERR_UNSUPPORTED.  q, k, v, o, partial_o must be 16-byte aligned.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device
+ * memory and keeps no state between calls besides a cached SM count per device.
+ * All device work is asynchronous on the given stream (a cudaStream_t passed as
+ * void*; NULL = legacy default stream).
+ *
+ * Errors: every entry point returns an fd_status (0 = FD_OK, negative =
+ * error) and never throws.  Arguments are validated on the host before any
+ * launch; launch failures return FD_ERR_CUDA.  Errors the kernels detect
+ * (a bounded wait that ran out, a derived index outside the plan) are written
+ * to a status word in the workspace and read by fd_get_device_status().
+ *
+ * Workspace: a caller-owned device buffer, zero-filled before its first use.
+ * Its first FD_WORKSPACE_HEADER_BYTES hold the device status word; fd_decode
+ * also keeps the split partials in it (size: fd_plan_info.workspace_bytes).
+ * Calls that share one workspace must be ordered on one stream.
+ */
+#ifndef FD_H
+#define FD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fd_status {
+    FD_OK = 0,
+    FD_ERR_INVALID_ARG = -1,   /* bad pointer, size, layout or indptr */
+    FD_ERR_UNSUPPORTED = -2,   /* head_dim or group size not built */
+    FD_ERR_WORKSPACE = -3,     /* workspace missing or too small */
+    FD_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
+    FD_ERR_TIMEOUT = -5,       /* an in-kernel wait ran past its limit */
+    FD_ERR_DEVICE_BOUNDS = -6  /* a kernel derived an index outside the plan */
+} fd_status;
+
+/* Keys per pipeline stage; every chunk length is a multiple of it. */
+#define FD_TILE_TOKENS 32
+/* Bytes at the start of every workspace reserved for the device status. */
+#define FD_WORKSPACE_HEADER_BYTES 256
+/* Default bound on each in-kernel wait, in nanoseconds. */
+#define FD_DEFAULT_TIMEOUT_NS 1000000000LL
+
+/*
+ * A decode plan (plain data; fill it with fd_plan).
+ *
+ * The plan fixes one chunk length C for the step.  Request b (L_b keys) is cut
+ * into splits_b = ceil(L_b / C) splits of equal length rounded up to a
+ * multiple of FD_TILE_TOKENS (the last one ragged); each (split, KV head) is
+ * one CTA of the split kernel.  The kernels re-derive each CTA's key range
+ * from kv_indptr on the device with this same rule, so no per-step work list
+ * is copied to the GPU.
+ */
+typedef struct fd_plan_info {
+    int32_t batch;
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t group_size;        /* num_qo_heads / num_kv_heads */
+    int32_t chunk;             /* max keys per split, multiple of FD_TILE_TOKENS */
+    int32_t total_splits;      /* sum over requests of splits_b */
+    int32_t max_splits;        /* max over requests of splits_b */
+    int32_t num_work;          /* split-kernel CTAs = total_splits * num_kv_heads */
+    int32_t num_partial_rows;  /* total_splits * num_qo_heads */
+    int32_t num_sms;           /* SM count the chunk was chosen for */
+    int32_t ctas_per_sm;       /* target CTAs per SM the chunk was chosen for */
+    int64_t total_tokens;      /* kv_indptr[batch] */
+    int64_t workspace_bytes;   /* workspace fd_decode needs for this plan */
+    int64_t timeout_ns;        /* limit on each in-kernel wait; 0 makes every
+                                  wait give up at once (a test hook: the call
+                                  then reports FD_ERR_TIMEOUT) */
+} fd_plan_info;
+
+/* Human-readable name of a status code (static string). */
+const char *fd_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int fd_version(void);
+
+/* SM count of a CUDA device (cached after the first query). */
+int fd_num_sms(int device, int *num_sms);
+
+/*
+ * fd_plan -- choose the chunk length and size the split grid (host only, no
+ * CUDA call unless num_sms == 0).
+ *
+ * Article §2 (split grid = batch x heads x chunks) and §6 (chunk size tuning
+ * guide: enough CTAs to fill the SMs, chunks not so small that the stage-2
+ * reduction dominates).  With chunk == 0 the plan takes
+ *     C = max(FD_MIN_CHUNK, roundup(ceil(T * Hkv / (num_sms * ctas_per_sm)), FD_TILE_TOKENS))
+ * so the grid covers about ctas_per_sm CTAs per SM; chunk > 0 forces C (must be
+ * a positive multiple of FD_TILE_TOKENS).
+ *
+ * kv_indptr_host: host int32 [batch+1].  num_sms: 0 = query the current
+ * device.  ctas_per_sm: 0 = default (2).  Writes *info; returns
+ * FD_ERR_INVALID_ARG for a malformed indptr or head counts,
+ * FD_ERR_UNSUPPORTED for an unsupported head_dim or group size.
+ */
+#define FD_MIN_CHUNK 128
+int fd_plan(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+            const int32_t *kv_indptr_host, int num_sms, int ctas_per_sm, int chunk,
+            fd_plan_info *info);
+
+/*
+ * fd_plan_work_items -- list the plan's CTAs in launch order (host only).
+ * items: caller-owned host int32 [num_work][5] = (b, kv_head, split,
+ * tok_begin, tok_end) with absolute key rows [tok_begin, tok_end).
+ * capacity: rows available in items; FD_ERR_INVALID_ARG if too small.
+ */
+int fd_plan_work_items(const fd_plan_info *info, const int32_t *kv_indptr_host,
+                       int32_t *items, int64_t capacity);
+
+/*
+ * fd_decode_split -- stage 1 (article §3, "local chunk computation"): one CTA
+ * per (split, KV head) streams its keys once through shared memory (TMA,
+ * multi-stage mbarrier pipeline), and for each of the G query heads that share
+ * the KV head computes the local max, the local exp-sum and the local
+ * probability-weighted sum of V.  It stores the partial in normalised form,
+ *     partial_o   = (sum_j exp(s_j - m) V_j) / (sum_j exp(s_j - m))
+ *     partial_lse = m + ln(sum_j exp(s_j - m)),
+ * which carries the same information as the article's (output, max, sum).
+ *
+ * info: from fd_plan for this kv_indptr.  kv_indptr_dev: device copy of the
+ * same indptr.  scale: softmax scale (applied to q.k).  workspace: device,
+ * >= FD_WORKSPACE_HEADER_BYTES (status word).
+ */
+int fd_decode_split(const fd_plan_info *info, const void *q, const void *k,
+                    const void *v, const int32_t *kv_indptr_dev, float scale,
+                    float *partial_o, float *partial_lse, void *workspace,
+                    int64_t workspace_bytes, void *stream);
+
+/*
+ * fd_merge -- stage 2 (article §3, "global reduction"): for each (b, hq) take
+ * M = max_i partial_lse_i, weights w_i = exp(partial_lse_i - M), and write
+ *     o = sum_i w_i partial_o_i / sum_i w_i,   lse = M + ln sum_i w_i.
+ * A request with no keys gets o = 0, lse = -inf.
+ */
+int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
+             const float *partial_o, const float *partial_lse, float *o, float *lse,
+             void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
+ * fd_decode -- plan (default chunking for the current device), stage 1 and
+ * stage 2 in one call; the partials live in the workspace, which must hold
+ * fd_plan_info.workspace_bytes (FD_ERR_WORKSPACE otherwise; query it with
+ * fd_plan for the same arguments).  Needs kv_indptr on the host (for the plan)
+ * and on the device (for the kernels); the two must hold the same values.
+ */
+int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+              const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+              const void *q, const void *k, const void *v, float scale,
+              float *o, float *lse, void *workspace, int64_t workspace_bytes,
+              void *stream);
+
+/*
+ * fd_get_device_status -- synchronise the stream, read and clear the status
+ * word the kernels write into the workspace.  Returns FD_OK,
+ * FD_ERR_TIMEOUT, FD_ERR_DEVICE_BOUNDS, or FD_ERR_CUDA if the read failed.
+ */
+int fd_get_device_status(void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H */

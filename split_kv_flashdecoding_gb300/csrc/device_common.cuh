@@ -1,0 +1,200 @@
+// device_common.cuh -- sm_103a building blocks shared by the libfd kernels:
+// mbarrier and TMA (cp.async.bulk.tensor) wrappers in inline PTX, bounded
+// waits, bf16 unpacking, warp reductions, and the on-device derivation of a
+// CTA's split from kv_indptr (the same rule as the host planner).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fd.h"
+#include "plan_rule.h"
+
+namespace fd {
+
+constexpr int kHeadDim = 128;
+constexpr int kTile = FD_TILE_TOKENS;   // keys per pipeline stage
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// A wait that drains copies still in flight after an error always gets this
+// long, whatever the plan's timeout (the copies target valid addresses and end).
+constexpr int64_t kDrainTimeoutNs = 200000000LL;
+
+// ------------------------------------------------------------------ status
+
+// Record the first error a kernel hits in the workspace status word.
+__device__ __forceinline__ void report(int *status, int code)
+{
+    atomicCAS(status, 0, code);
+}
+
+// ----------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete; give up after
+// timeout_ns (timeout_ns <= 0 gives up at once).  Returns false on give-up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t timeout_ns)
+{
+    if (timeout_ns <= 0)
+        return false;
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((int64_t)(global_timer_ns() - t0) > timeout_ns)
+            return false;
+    }
+}
+
+// --------------------------------------------------------------------- TMA
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled TMA load of box (x, y) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                            int32_t y, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// ------------------------------------------------------------ arithmetic
+
+// Two packed bf16 (low half = first element) widened exactly to fp32.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// ------------------------------------------------------- split derivation
+
+struct SplitCoord {
+    int32_t b;        // request
+    int32_t prefix;   // splits of requests before b
+    int32_t splits;   // splits_b
+    int32_t s;        // split within the request (when derived from a split index)
+    int32_t beg, end; // the request's key rows
+};
+
+// Warp-collective: locate global split `j` (if by_request is false) or request
+// `j` (if true) by scanning kv_indptr.  All lanes return the same result;
+// returns false if j is out of range.
+__device__ __forceinline__ bool derive_split(const int32_t *__restrict__ kv_indptr, int batch,
+                                             int32_t chunk, int32_t j, bool by_request,
+                                             SplitCoord &out)
+{
+    const int lane = threadIdx.x & 31;
+    int32_t carry = 0;
+    for (int base = 0; base < batch; base += 32) {
+        const int b = base + lane;
+        int32_t beg = 0, end = 0, n = 0;
+        if (b < batch) {
+            beg = __ldg(kv_indptr + b);
+            end = __ldg(kv_indptr + b + 1);
+            n = splits_for(end - beg, chunk);
+        }
+        int32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += t;
+        }
+        incl += carry;
+        const int32_t excl = incl - n;
+        const bool hit = b < batch && (by_request ? b == j : (j >= excl && j < incl));
+        const unsigned mask = __ballot_sync(0xffffffffu, hit);
+        if (mask) {
+            const int src = __ffs(mask) - 1;
+            out.b = __shfl_sync(0xffffffffu, b, src);
+            out.prefix = __shfl_sync(0xffffffffu, excl, src);
+            out.splits = __shfl_sync(0xffffffffu, n, src);
+            out.beg = __shfl_sync(0xffffffffu, beg, src);
+            out.end = __shfl_sync(0xffffffffu, end, src);
+            out.s = by_request ? 0 : j - out.prefix;
+            return true;
+        }
+        carry = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return false;
+}
+
+}  // namespace fd

@@ -1,0 +1,244 @@
+// fd_api.cu -- the C ABI of libfd: argument checks, TMA descriptors and the
+// launches of the two kernels.  See include/fd.h for the contract of each
+// entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "fd.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kHeadDim = 128;
+constexpr int kBoxCols = 64;     // one 128-byte swizzle span of bf16
+constexpr int kBoxRows = FD_TILE_TOKENS;
+
+bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+int64_t round_up(int64_t x, int64_t m)
+{
+    return (x + m - 1) / m * m;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// K or V [T, Hkv, 128] bf16 seen as a 2-D tensor of T rows x Hkv*128 columns;
+// one box = 32 rows x 64 columns, 128-byte swizzle, zero fill past row T.
+int make_kv_map(CUtensorMap *map, const void *base, int64_t total_tokens, int num_kv_heads)
+{
+    auto encode = tensor_map_encoder();
+    if (!encode)
+        return FD_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * kHeadDim, (cuuint64_t)total_tokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * kHeadDim * 2};
+    const cuuint32_t box[2] = {kBoxCols, kBoxRows};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                              dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
+}
+
+int check_info(const fd_plan_info *info)
+{
+    if (!info)
+        return FD_ERR_INVALID_ARG;
+    if (info->head_dim != kHeadDim)
+        return FD_ERR_UNSUPPORTED;
+    if (info->batch < 0 || info->num_qo_heads <= 0 || info->num_kv_heads <= 0 ||
+        info->num_qo_heads % info->num_kv_heads != 0 ||
+        info->group_size != info->num_qo_heads / info->num_kv_heads)
+        return FD_ERR_INVALID_ARG;
+    const int g = info->group_size;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return FD_ERR_UNSUPPORTED;
+    if (info->chunk <= 0 || info->chunk % FD_TILE_TOKENS != 0 || info->total_splits < 0 ||
+        (int64_t)info->num_work != (int64_t)info->total_splits * info->num_kv_heads ||
+        (int64_t)info->num_partial_rows != (int64_t)info->total_splits * info->num_qo_heads ||
+        info->total_tokens < 0 || info->total_tokens > INT32_MAX)
+        return FD_ERR_INVALID_ARG;
+    return FD_OK;
+}
+
+cudaStream_t as_stream(void *s)
+{
+    return reinterpret_cast<cudaStream_t>(s);
+}
+
+}  // namespace
+
+extern "C" const char *fd_status_string(int status)
+{
+    switch (status) {
+    case FD_OK: return "FD_OK";
+    case FD_ERR_INVALID_ARG: return "FD_ERR_INVALID_ARG";
+    case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED";
+    case FD_ERR_WORKSPACE: return "FD_ERR_WORKSPACE";
+    case FD_ERR_CUDA: return "FD_ERR_CUDA";
+    case FD_ERR_TIMEOUT: return "FD_ERR_TIMEOUT";
+    case FD_ERR_DEVICE_BOUNDS: return "FD_ERR_DEVICE_BOUNDS";
+    default: return "FD_ERR_UNKNOWN";
+    }
+}
+
+extern "C" int fd_version(void)
+{
+    return 100;   // 0.1.0
+}
+
+extern "C" int fd_num_sms(int device, int *num_sms)
+{
+    static int cache[64] = {};
+    if (!num_sms)
+        return FD_ERR_INVALID_ARG;
+    if (device < 0 && cudaGetDevice(&device) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (device < 64 && cache[device] > 0) {
+        *num_sms = cache[device];
+        return FD_OK;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
+        return FD_ERR_CUDA;
+    if (device < 64)
+        cache[device] = n;
+    *num_sms = n;
+    return FD_OK;
+}
+
+extern "C" int fd_decode_split(const fd_plan_info *info, const void *q, const void *k,
+                               const void *v, const int32_t *kv_indptr_dev, float scale,
+                               float *partial_o, float *partial_lse, void *workspace,
+                               int64_t workspace_bytes, void *stream)
+{
+    int rc = check_info(info);
+    if (rc != FD_OK)
+        return rc;
+    if (!workspace || workspace_bytes < FD_WORKSPACE_HEADER_BYTES)
+        return FD_ERR_WORKSPACE;
+    if (info->num_work == 0)
+        return FD_OK;
+    if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
+        return FD_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(partial_o, 16) ||
+        !aligned(partial_lse, 4) || !aligned(kv_indptr_dev, 4) || !aligned(workspace, 16))
+        return FD_ERR_INVALID_ARG;
+    if (!(scale == scale))
+        return FD_ERR_INVALID_ARG;
+
+    CUtensorMap tm_k, tm_v;
+    if ((rc = make_kv_map(&tm_k, k, info->total_tokens, info->num_kv_heads)) != FD_OK ||
+        (rc = make_kv_map(&tm_v, v, info->total_tokens, info->num_kv_heads)) != FD_OK)
+        return rc;
+
+    fd::SplitParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.kv_indptr = kv_indptr_dev;
+    p.partial_o = partial_o;
+    p.partial_lse = partial_lse;
+    p.status = static_cast<int *>(workspace);
+    p.batch = info->batch;
+    p.num_qo_heads = info->num_qo_heads;
+    p.num_kv_heads = info->num_kv_heads;
+    p.chunk = info->chunk;
+    p.num_partial_rows = info->num_partial_rows;
+    p.total_tokens = (int32_t)info->total_tokens;
+    p.q_scale = scale * 1.4426950408889634f;
+    p.timeout_ns = info->timeout_ns;
+    const cudaError_t e =
+        fd::launch_split(tm_k, tm_v, p, info->group_size, info->num_work, as_stream(stream));
+    return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+extern "C" int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
+                        const float *partial_o, const float *partial_lse, float *o, float *lse,
+                        void *workspace, int64_t workspace_bytes, void *stream)
+{
+    const int rc = check_info(info);
+    if (rc != FD_OK)
+        return rc;
+    if (!workspace || workspace_bytes < FD_WORKSPACE_HEADER_BYTES)
+        return FD_ERR_WORKSPACE;
+    if (info->batch == 0)
+        return FD_OK;
+    if (!kv_indptr_dev || !o || !lse || (info->num_partial_rows > 0 && (!partial_o || !partial_lse)))
+        return FD_ERR_INVALID_ARG;
+    if (!aligned(o, 16) || !aligned(lse, 4) || !aligned(partial_o, 16) ||
+        !aligned(partial_lse, 4) || !aligned(kv_indptr_dev, 4) || !aligned(workspace, 16))
+        return FD_ERR_INVALID_ARG;
+    fd::MergeParams p;
+    p.kv_indptr = kv_indptr_dev;
+    p.partial_o = partial_o;
+    p.partial_lse = partial_lse;
+    p.o = o;
+    p.lse = lse;
+    p.status = static_cast<int *>(workspace);
+    p.batch = info->batch;
+    p.num_qo_heads = info->num_qo_heads;
+    p.chunk = info->chunk;
+    p.num_partial_rows = info->num_partial_rows;
+    const cudaError_t e = fd::launch_merge(p, as_stream(stream));
+    return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                         const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+                         const void *q, const void *k, const void *v, float scale, float *o,
+                         float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    fd_plan_info info;
+    int rc = fd_plan(batch, num_qo_heads, num_kv_heads, head_dim, kv_indptr_host, 0, 0, 0, &info);
+    if (rc != FD_OK)
+        return rc;
+    if (!workspace || workspace_bytes < info.workspace_bytes)
+        return FD_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *partial_lse = reinterpret_cast<float *>(ws + FD_WORKSPACE_HEADER_BYTES);
+    float *partial_o = reinterpret_cast<float *>(
+        ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)info.num_partial_rows * 4, 256));
+    rc = fd_decode_split(&info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
+                         workspace_bytes, stream);
+    if (rc != FD_OK)
+        return rc;
+    return fd_merge(&info, kv_indptr_dev, partial_o, partial_lse, o, lse, workspace,
+                    workspace_bytes, stream);
+}
+
+extern "C" int fd_get_device_status(void *workspace, void *stream)
+{
+    if (!workspace)
+        return FD_ERR_WORKSPACE;
+    int status = 0;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(&status, workspace, sizeof status, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (status != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof status, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return FD_ERR_CUDA;
+    }
+    return status;
+}

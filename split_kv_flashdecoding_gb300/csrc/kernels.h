@@ -1,0 +1,46 @@
+// kernels.h -- parameters and launchers of the libfd kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fd {
+
+struct SplitParams {
+    const uint16_t *q;          // bf16 [B, Hq, D]
+    const int32_t *kv_indptr;   // device [B+1]
+    float *partial_o;           // [rows, D]
+    float *partial_lse;         // [rows]
+    int *status;                // workspace status word
+    int32_t batch;
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t chunk;
+    int32_t num_partial_rows;
+    int32_t total_tokens;
+    float q_scale;              // softmax scale * log2(e): logits are kept in base 2
+    int64_t timeout_ns;
+};
+
+struct MergeParams {
+    const int32_t *kv_indptr;
+    const float *partial_o;
+    const float *partial_lse;
+    float *o;                   // [B, Hq, D]
+    float *lse;                 // [B, Hq]
+    int *status;
+    int32_t batch;
+    int32_t num_qo_heads;
+    int32_t chunk;
+    int32_t num_partial_rows;
+};
+
+// Stage 1: one CTA per (split, KV head); grid = num_work.
+cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
+                         int group, int num_work, cudaStream_t stream);
+
+// Stage 2: one CTA per (request, query head).
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
+
+}  // namespace fd
