@@ -44,20 +44,27 @@ def _stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/ into _build/libfd.so if anything changed; return its path."""
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str | None = None) -> str:
+    """Compile csrc/ into _build/libfd.so if anything changed; return its path.
+
+    defines/out build a variant (extra -D flags) into another file instead,
+    e.g. to compare launch shapes.
+    """
+    if out is None and not force and not _stale():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    lib_path = out or LIB
+    build_dir = os.path.dirname(lib_path) if out else BUILD
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC, "-Xcompiler", "-fPIC"]
+    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC, "-Xcompiler", "-fPIC",
+              *[f"-D{d}" for d in defines]]
     jobs = []
     for src in CUDA_SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         jobs.append([nvcc, *ARCH, "-lineinfo", *common, "-Xptxas", "-v" if verbose else "-O3",
                      "-c", os.path.join(CSRC, src), "-o", obj])
     for src in HOST_SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         jobs.append([nvcc, *common, "-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj])
 
     def run(cmd):
@@ -72,11 +79,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for log in logs:
             if log.strip():
                 print(log)
-    objs = [os.path.join(BUILD, s + ".o") for s in CUDA_SOURCES + HOST_SOURCES]
-    tmp = LIB + f".tmp{os.getpid()}"
+    objs = [os.path.join(build_dir, s + ".o") for s in CUDA_SOURCES + HOST_SOURCES]
+    tmp = lib_path + f".tmp{os.getpid()}"
     run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lpthread", "-lrt"])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -120,6 +120,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Allow the next grid in the stream (launched with programmatic stream
+// serialisation) to start launching; its griddep_wait() still waits for this
+// grid to finish and its writes to be visible.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding grid in the stream has completed (no-op when this
+// grid was not launched as a programmatic dependent).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------ arithmetic
 
 // Two packed bf16 (low half = first element) widened exactly to fp32.

@@ -40,7 +40,11 @@ struct MergeParams {
 cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
                          int group, int num_work, cudaStream_t stream);
 
-// Stage 2: one CTA per (request, query head).
+// Resident split-kernel CTAs per SM the launch shape is built for.
+int split_ctas_per_sm();
+
+// Stage 2: one CTA per (request, query head), launched as a programmatic
+// dependent of the preceding grid so its launch overlaps that grid's tail.
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 
 }  // namespace fd

@@ -9,7 +9,9 @@
 // w_i = exp(LSE_i - M); the output LSE is M + ln sum_i w_i.
 //
 // One CTA (4 warps) per (request, query head).  Warp w accumulates splits
-// w, w+4, ...; lane = 4 output columns (one float4 of a 512-byte partial row).
+// w, w+4, ... with a running maximum (8 rows of loads in flight), lane = 4
+// output columns (one float4 of a 512-byte partial row); the four warp states
+// are combined with the same rescaling.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -19,11 +21,12 @@ namespace fd {
 namespace {
 
 constexpr int kMergeWarps = 4;
+constexpr int kBatch = 8;   // partial rows a warp loads at once
 
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p)
 {
     __shared__ int32_t s_info[3];   // prefix, splits, ok
-    __shared__ float s_max[kMergeWarps];
+    __shared__ float s_m[kMergeWarps];
     __shared__ float s_den[kMergeWarps];
     __shared__ float4 s_acc[kMergeWarps][32];
 
@@ -45,6 +48,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
                 report(p.status, FD_ERR_DEVICE_BOUNDS);
         }
     }
+    // Partials are written by the preceding split grid: wait for it here.
+    griddep_wait();
     __syncthreads();
     if (!s_info[2])
         return;
@@ -60,47 +65,70 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     }
     const int64_t base = partial_row(s_info[0], p.num_qo_heads, hq, n, 0);
     const float *lse_in = p.partial_lse + base;
+    const float4 *o_in = reinterpret_cast<const float4 *>(p.partial_o + base * kHeadDim) + lane;
 
-    // global max of the chunk statistics
-    float mx = -INFINITY;
-    for (int i = tid; i < n; i += kMergeWarps * 32)
-        mx = fmaxf(mx, lse_in[i]);
-    mx = warp_max(mx);
-    if (lane == 0)
-        s_max[warp] = mx;
-    __syncthreads();
-    mx = s_max[0];
-#pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w)
-        mx = fmaxf(mx, s_max[w]);
-
-    // rescaled sums
-    float den = 0.f;
+    // Warp w reduces rows w, w + 4, ... with a running maximum, kBatch rows of
+    // loads in flight at a time.
+    float m = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = warp; i < n; i += kMergeWarps) {
-        const float w = expf(lse_in[i] - mx);
-        const float4 v = reinterpret_cast<const float4 *>(p.partial_o + (base + i) * kHeadDim)[lane];
-        den += w;
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+    for (int i0 = warp; i0 < n; i0 += kMergeWarps * kBatch) {
+        float l[kBatch];
+        float4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kMergeWarps;
+            if (i < n) {
+                l[u] = __ldg(lse_in + i);
+                v[u] = __ldg(o_in + (int64_t)i * (kHeadDim / 4));
+            } else {
+                l[u] = -INFINITY;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float bm = l[0];
+#pragma unroll
+        for (int u = 1; u < kBatch; ++u)
+            bm = fmaxf(bm, l[u]);
+        const float m_new = fmaxf(m, bm);   // finite: row i0 exists
+        const float f = expf(m - m_new);
+        den *= f;
+        acc.x *= f;
+        acc.y *= f;
+        acc.z *= f;
+        acc.w *= f;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const float w = expf(l[u] - m_new);
+            den += w;
+            acc.x = fmaf(w, v[u].x, acc.x);
+            acc.y = fmaf(w, v[u].y, acc.y);
+            acc.z = fmaf(w, v[u].z, acc.z);
+            acc.w = fmaf(w, v[u].w, acc.w);
+        }
+        m = m_new;
     }
     s_acc[warp][lane] = acc;
-    if (lane == 0)
+    if (lane == 0) {
+        s_m[warp] = m;
         s_den[warp] = den;
+    }
     __syncthreads();
     if (warp == 0) {
+        float mx = s_m[0];
+#pragma unroll
+        for (int w = 1; w < kMergeWarps; ++w)
+            mx = fmaxf(mx, s_m[w]);
         float d = 0.f;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kMergeWarps; ++w) {
-            d += s_den[w];
+            const float f = expf(s_m[w] - mx);   // 0 for a warp that had no rows
+            d = fmaf(f, s_den[w], d);
             const float4 t = s_acc[w][lane];
-            a.x += t.x;
-            a.y += t.y;
-            a.z += t.z;
-            a.w += t.w;
+            a.x = fmaf(f, t.x, a.x);
+            a.y = fmaf(f, t.y, a.y);
+            a.z = fmaf(f, t.z, a.z);
+            a.w = fmaf(f, t.w, a.w);
         }
         const float inv = 1.f / d;
         reinterpret_cast<float4 *>(o_row)[lane] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
@@ -116,8 +144,17 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream)
     const int64_t ctas = (int64_t)p.batch * p.num_qo_heads;
     if (ctas == 0)
         return cudaSuccess;
-    merge_kernel<<<(unsigned)ctas, kMergeWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
 }
 
 }  // namespace fd

@@ -10,9 +10,11 @@
 #include "fd.h"
 #include "plan_rule.h"
 
-namespace {
+namespace fd {
+int split_ctas_per_sm();   // resident CTAs per SM of the split kernel's launch shape
+}
 
-constexpr int kDefaultCtasPerSm = 2;
+namespace {
 
 bool supported_group(int g)
 {
@@ -53,7 +55,7 @@ extern "C" int fd_plan(int batch, int num_qo_heads, int num_kv_heads, int head_d
             return rc;
     }
     if (ctas_per_sm == 0)
-        ctas_per_sm = kDefaultCtasPerSm;
+        ctas_per_sm = fd::split_ctas_per_sm();
 
     const int64_t total = kv_indptr_host[batch];
     int64_t c = chunk;

@@ -17,14 +17,23 @@
 //   warps 0..NC-1 (consumers): warp w takes tiles w, w+NC, ...  NS is a
 //     multiple of NC, so every stage always goes to the same warp and a warp
 //     never waits on a barrier more than one phase ahead (parity waits can only
-//     tell two phases apart).  Each warp keeps its own online-softmax state (running max m, partial sums l, accumulator) for
-//     the G heads.  Scores: lane = key, q from shared memory (broadcast),
-//     packed fp32x2 FMAs.  P.V: lane = 4 consecutive output columns, p values
-//     broadcast from shared memory.  At the end the NC warp states are merged
-//     in shared memory (the same rescaling as stage 2) and the normalised
-//     partial (O_i, LSE_i) is written.
-// Logits are kept in base 2 (q pre-multiplied by scale * log2 e); the stored
-// LSE is converted back to the natural log.
+//     tell two phases apart).  Each warp keeps its own online-softmax state and
+//     at the end the NC states are merged in shared memory with the same
+//     rescaling as stage 2.
+//
+// Arithmetic per tile (warp-level mma.sync m16n8k16, bf16 in, fp32 accumulate):
+//   S = Q K^T    A = the G query rows (rows >= G are zero), kept in registers;
+//                B = K rows read with ldmatrix straight from the swizzled tile.
+//   online softmax on the fp32 accumulator fragments (base-2 logits: S is
+//                scaled by scale * log2 e; the running max and sum are per row).
+//   O += P V     A = P split into bf16 hi + lo parts: rows 0-7 carry hi, rows
+//                8-15 (padding in the score product) carry lo = P - hi, so the
+//                weights keep ~16 mantissa bits; O rows g and g+8 are added at
+//                the end.  B = V rows read with ldmatrix.trans.
+// The tensor cores are used here because the CUDA-core version of the same
+// loop was limited by shared-memory wavefronts (broadcast reads of q and p)
+// and instruction issue, not by HBM; the contraction itself stays tiny
+// (m = G <= 8 rows).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,15 +45,15 @@ namespace {
 
 constexpr int kHalfBytes = kTile * 128;        // 32 keys x 64 bf16 (one swizzled box)
 constexpr int kStageBytes = 4 * kHalfBytes;    // K lo, K hi, V lo, V hi
+constexpr int kMaxGroup = 8;                   // rows 8-15 of the MMA carry the lo part of P
 
 enum Misc { kB, kPrefix, kSplits, kS, kT0, kT1, kOk, kAbort, kIssued, kMiscCount };
 
 template <int G, int NC, int NS>
 struct Layout {
     static_assert(NS % NC == 0, "each stage must belong to one consumer warp");
-    static constexpr int kOffQ = NS * kStageBytes;
-    static constexpr int kOffP = kOffQ + G * kHeadDim * 4;
-    static constexpr int kOffBar = kOffP + NC * kTile * G * 8;
+    static_assert(G >= 1 && G <= kMaxGroup, "group size");
+    static constexpr int kOffBar = NS * kStageBytes;
     static constexpr int kOffMisc = kOffBar + 2 * NS * 8;
     static constexpr int kBytes = kOffMisc + kMiscCount * 4;
     static constexpr int kAlloc = kBytes + 1024;   // room to align the base to 1024 B
@@ -54,30 +63,41 @@ struct Layout {
     static_assert(kOffCombL + NC * G * 4 <= NS * kStageBytes, "combine area must fit the ring");
 };
 
-// One key row of P.V for all G heads: acc[g] += p[g] * v (4 columns per lane).
-template <int G>
-__device__ __forceinline__ void pv_step(const uint8_t *v_half, int cc, int sub, int r,
-                                        const float2 *__restrict__ p_row, float2 (&acc)[G][2])
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
-    const uint2 vw =
-        *reinterpret_cast<const uint2 *>(v_half + r * 128 + ((cc ^ (r & 7)) << 4) + sub);
-    const float2 v0 = bf16x2_to_float2(vw.x);
-    const float2 v1 = bf16x2_to_float2(vw.y);
-    if constexpr (G == 1) {
-        const float2 pp = p_row[0];
-        acc[0][0] = __ffma2_rn(v0, pp, acc[0][0]);
-        acc[0][1] = __ffma2_rn(v1, pp, acc[0][1]);
-    } else {
-#pragma unroll
-        for (int g = 0; g < G; g += 2) {
-            const float4 pq = *reinterpret_cast<const float4 *>(p_row + g);
-            const float2 p0 = make_float2(pq.x, pq.y), p1 = make_float2(pq.z, pq.w);
-            acc[g][0] = __ffma2_rn(v0, p0, acc[g][0]);
-            acc[g][1] = __ffma2_rn(v1, p0, acc[g][1]);
-            acc[g + 1][0] = __ffma2_rn(v0, p1, acc[g + 1][0]);
-            acc[g + 1][1] = __ffma2_rn(v1, p1, acc[g + 1][1]);
-        }
-    }
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D (+)= A B for one m16n8k16 tile, bf16 inputs, fp32 accumulator.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> packed bf16x2 (first argument in the low half), round to nearest.
+__device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo_elem, hi_elem);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float bf16_round(float x)
+{
+    return __bfloat162float(__float2bfloat16_rn(x));
 }
 
 template <int G, int NC, int NS, int MIN_CTAS>
@@ -89,8 +109,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *q_s = reinterpret_cast<float *>(smem + L::kOffQ);
-    float2 *p_s = reinterpret_cast<float2 *>(smem + L::kOffP);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     volatile int *misc = reinterpret_cast<volatile int *>(smem + L::kOffMisc);
 
@@ -98,8 +116,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     const int kvh = blockIdx.x % p.num_kv_heads;
     const int32_t j = blockIdx.x / p.num_kv_heads;
 
-    // ---- locate this CTA's split (same rule as the host planner)
-    if (warp == 0) {
+    // ---- the producer warp locates this CTA's split (same rule as the host
+    // planner), sets up the barriers and puts the first NS tiles in flight
+    // before the block synchronises, so the loads start as early as possible.
+    const int32_t x_col = kvh * kHeadDim;
+    uint64_t pol = 0;
+    int issued = 0;
+    if (warp == NC) {
         SplitCoord c{};
         bool ok = derive_split(p.kv_indptr, p.batch, p.chunk, j, false, c);
         if (lane == 0) {
@@ -120,19 +143,29 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
             misc[kT1] = t1;
             misc[kOk] = ok;
             misc[kAbort] = 0;
-            misc[kIssued] = 0;
-            if (!ok)
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(smem_addr(&bars[s]), 1);        // full: producer arrive + TMA bytes
+                mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: consumer warp releases
+            }
+            fence_mbar_init();
+            if (!ok) {
                 report(p.status, FD_ERR_DEVICE_BOUNDS);
+            } else {
+                pol = l2_evict_first_policy();
+                const int first = min(NS, (t1 - t0 + kTile - 1) / kTile);
+                for (; issued < first; ++issued) {
+                    const uint32_t full = smem_addr(&bars[issued]);
+                    const uint32_t dst = smem_addr(smem + issued * kStageBytes);
+                    const int32_t y = t0 + issued * kTile;
+                    mbar_arrive_expect_tx(full, kStageBytes);
+                    tma_load_2d(dst, &tm_k, x_col, y, full, pol);
+                    tma_load_2d(dst + kHalfBytes, &tm_k, x_col + 64, y, full, pol);
+                    tma_load_2d(dst + 2 * kHalfBytes, &tm_v, x_col, y, full, pol);
+                    tma_load_2d(dst + 3 * kHalfBytes, &tm_v, x_col + 64, y, full, pol);
+                }
+            }
+            misc[kIssued] = issued;
         }
-    }
-    if (warp == NC && lane == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(smem_addr(&bars[s]), 1);        // full: producer arrive + TMA bytes
-            mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: consumer warp releases
-        }
-        fence_mbar_init();
-        tma_prefetch_map(&tm_k);
-        tma_prefetch_map(&tm_v);
     }
     __syncthreads();
     if (!misc[kOk])
@@ -141,43 +174,21 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     const int n_tiles = (t1 - t0 + kTile - 1) / kTile;
     const int b = misc[kB];
 
-    // ---- q of the G heads -> shared memory, fp32, times scale*log2(e)
-    if (warp < NC) {
-        for (int i = tid; i < G * 16; i += NC * 32) {
-            const int g = i >> 4, c = i & 15;
-            const uint4 w = *reinterpret_cast<const uint4 *>(
-                p.q + ((int64_t)b * p.num_qo_heads + kvh * G + g) * kHeadDim + c * 8);
-            float *dst = q_s + g * kHeadDim + c * 8;
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    // Per-thread fragment coordinates: row g = lane / 4 of the MMA tiles,
+    // column pair 2 * (lane % 4).
+    const int g_row = lane >> 2, t4 = lane & 3;
+    float m_run = -INFINITY, l_part = 0.f;
+    float o_acc[16][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = bf16x2_to_float2(ws[e]);
-                dst[2 * e] = f.x * p.q_scale;
-                dst[2 * e + 1] = f.y * p.q_scale;
-            }
-        }
-    }
-    __syncthreads();
-
-    float m_run[G], l_part[G];
-    float2 acc[G][2];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m_run[g] = -INFINITY;
-        l_part[g] = 0.f;
-        acc[g][0] = acc[g][1] = make_float2(0.f, 0.f);
-    }
+    for (int n = 0; n < 16; ++n)
+        o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
 
     if (warp == NC) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            const int32_t x = kvh * kHeadDim;
-            int issued = 0;
-            for (int i = 0; i < n_tiles; ++i) {
+            for (int i = issued; i < n_tiles; ++i) {
                 const int s = i % NS;
-                if (i >= NS &&
-                    !mbar_wait(smem_addr(&bars[NS + s]), ((i / NS) - 1) & 1, p.timeout_ns)) {
+                if (!mbar_wait(smem_addr(&bars[NS + s]), ((i / NS) - 1) & 1, p.timeout_ns)) {
                     misc[kAbort] = 1;
                     report(p.status, FD_ERR_TIMEOUT);
                     break;
@@ -188,19 +199,35 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                 const uint32_t dst = smem_addr(smem + s * kStageBytes);
                 const int32_t y = t0 + i * kTile;
                 mbar_arrive_expect_tx(full, kStageBytes);
-                tma_load_2d(dst, &tm_k, x, y, full, pol);
-                tma_load_2d(dst + kHalfBytes, &tm_k, x + 64, y, full, pol);
-                tma_load_2d(dst + 2 * kHalfBytes, &tm_v, x, y, full, pol);
-                tma_load_2d(dst + 3 * kHalfBytes, &tm_v, x + 64, y, full, pol);
+                tma_load_2d(dst, &tm_k, x_col, y, full, pol);
+                tma_load_2d(dst + kHalfBytes, &tm_k, x_col + 64, y, full, pol);
+                tma_load_2d(dst + 2 * kHalfBytes, &tm_v, x_col, y, full, pol);
+                tma_load_2d(dst + 3 * kHalfBytes, &tm_v, x_col + 64, y, full, pol);
                 issued = i + 1;
             }
             misc[kIssued] = issued;
         }
     } else {
         // ---------------------------------------------------------- consumers
-        float2 *p_w = p_s + warp * kTile * G;       // [key][g] pairs (p, p)
-        const int sw = lane & 7;
-        const int cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
+        // Q fragments (A operand of S = Q K^T) for the 8 k-steps of 16 columns;
+        // rows g >= G and the padding rows 8-15 are zero.
+        uint32_t qa[8][2];
+        {
+            const bool valid = g_row < G;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                p.q + ((int64_t)b * p.num_qo_heads + kvh * G + (valid ? g_row : 0)) * kHeadDim);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                qa[kk][0] = valid ? __ldg(qrow + kk * 8 + t4) : 0u;       // cols 16kk + 2t4 (+1)
+                qa[kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + t4) : 0u;   // cols 16kk + 8 + 2t4 (+1)
+            }
+        }
+        const float qk_scale = p.q_scale;
+        // ldmatrix: lane supplies row lr of matrix lm.  The 128-byte swizzle XORs
+        // the 16-byte chunk index with the row index mod 8, which is lr here.
+        const int lr = lane & 7, lm = lane >> 3;
+        const uint32_t ring = smem_addr(smem);
+
         for (int i = warp; i < n_tiles; i += NC) {
             const int s = i % NS;
             if (!mbar_wait(smem_addr(&bars[s]), (i / NS) & 1, p.timeout_ns)) {
@@ -208,64 +235,90 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                 report(p.status, FD_ERR_TIMEOUT);
                 break;
             }
-            const uint8_t *st = smem + s * kStageBytes;
+            const uint32_t st = ring + s * kStageBytes;
             const int n_valid = min(kTile, t1 - (t0 + i * kTile));
 
-            // scores: lane = key (row `lane` of the tile)
-            float sc[G];
-            {
-                const uint8_t *k_lo = st + lane * 128;
-                const uint8_t *k_hi = st + kHalfBytes + lane * 128;
-                float2 a0[G], a1[G];
+            // ---- S = Q K^T : 4 key groups (n-tiles) of 8, 8 k-steps of 16 columns
+            float sc[4][4];
 #pragma unroll
-                for (int g = 0; g < G; ++g)
-                    a0[g] = a1[g] = make_float2(0.f, 0.f);
-#pragma unroll 4
-                for (int c = 0; c < 16; ++c) {
-                    const uint8_t *kr = c < 8 ? k_lo : k_hi;
-                    const uint4 kw = *reinterpret_cast<const uint4 *>(kr + (((c & 7) ^ sw) << 4));
-                    const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
-                    const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+            for (int jn = 0; jn < 4; ++jn)
+                sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(q_s + g * kHeadDim + c * 8);
-                        const float4 qb =
-                            *reinterpret_cast<const float4 *>(q_s + g * kHeadDim + c * 8 + 4);
-                        a0[g] = __ffma2_rn(k0, make_float2(qa.x, qa.y), a0[g]);
-                        a1[g] = __ffma2_rn(k1, make_float2(qa.z, qa.w), a1[g]);
-                        a0[g] = __ffma2_rn(k2, make_float2(qb.x, qb.y), a0[g]);
-                        a1[g] = __ffma2_rn(k3, make_float2(qb.z, qb.w), a1[g]);
-                    }
+            for (int kp = 0; kp < 4; ++kp) {           // 32 columns per ldmatrix.x4
+                const uint32_t half = st + (kp >> 1) * kHalfBytes;
+                const int chunk = 4 * (kp & 1) + lm;   // matrix lm = columns 8*lm .. +7
+#pragma unroll
+                for (int jn = 0; jn < 4; ++jn) {
+                    const int row = 8 * jn + lr;
+                    uint32_t kb[4];
+                    ldsm_x4(half + row * 128 + ((chunk ^ lr) << 4), kb);
+                    mma_bf16(sc[jn], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, kb[0], kb[1]);
+                    mma_bf16(sc[jn], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, kb[2], kb[3]);
                 }
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    sc[g] = lane < n_valid ? (a0[g].x + a0[g].y) + (a1[g].x + a1[g].y) : -INFINITY;
             }
 
-            // online softmax over this tile (running max is warp-uniform)
+            // ---- online softmax on row g_row (this thread's 8 scores of the tile)
+            float x[8];
+            float mt = -INFINITY;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float mn = fmaxf(m_run[g], warp_max(sc[g]));
-                const float alpha = exp2f(m_run[g] - mn);
-                const float pv = exp2f(sc[g] - mn);
-                l_part[g] = fmaf(l_part[g], alpha, pv);
-                const float2 a2 = make_float2(alpha, alpha);
-                acc[g][0] = __fmul2_rn(acc[g][0], a2);
-                acc[g][1] = __fmul2_rn(acc[g][1], a2);
-                m_run[g] = mn;
-                p_w[lane * G + g] = make_float2(pv, pv);
+            for (int jn = 0; jn < 4; ++jn)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = 8 * jn + 2 * t4 + e;
+                    const float v = key < n_valid ? sc[jn][e] * qk_scale : -INFINITY;
+                    x[2 * jn + e] = v;
+                    mt = fmaxf(mt, v);
+                }
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+            const float m_new = fmaxf(m_run, mt);
+            const float alpha = exp2f(m_run - m_new);
+            m_run = m_new;
+            float psum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                x[e] = exp2f(x[e] - m_new);
+                psum += x[e];
             }
-            __syncwarp();
+            l_part = fmaf(l_part, alpha, psum);
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o_acc[n][0] *= alpha;
+                    o_acc[n][1] *= alpha;
+                    o_acc[n][2] *= alpha;
+                    o_acc[n][3] *= alpha;
+                }
+            }
+            // P as the A operand: k-step ks covers keys 16ks .. 16ks+15 (n-tiles
+            // 2ks, 2ks+1); rows 0-7 hi, rows 8-15 lo.
+            uint32_t pa[2][4];
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const float p0 = x[4 * ks], p1 = x[4 * ks + 1];
+                const float p2 = x[4 * ks + 2], p3 = x[4 * ks + 3];
+                const float h0 = bf16_round(p0), h1 = bf16_round(p1);
+                const float h2 = bf16_round(p2), h3 = bf16_round(p3);
+                pa[ks][0] = pack_bf16(h0, h1);
+                pa[ks][1] = pack_bf16(p0 - h0, p1 - h1);
+                pa[ks][2] = pack_bf16(h2, h3);
+                pa[ks][3] = pack_bf16(p2 - h2, p3 - h3);
+            }
 
-            // P.V: lane = output columns 4*lane .. 4*lane+3
-            const uint8_t *v_half = st + 2 * kHalfBytes + (lane >> 4) * kHalfBytes;
-            if (n_valid == kTile) {
-#pragma unroll 8
-                for (int r = 0; r < kTile; ++r)
-                    pv_step<G>(v_half, cc, sub, r, p_w + r * G, acc);
-            } else {
-                for (int r = 0; r < n_valid; ++r)
-                    pv_step<G>(v_half, cc, sub, r, p_w + r * G, acc);
+            // ---- O += P V : 2 k-steps of 16 keys, 16 n-tiles of 8 columns
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int row = 16 * ks + 8 * (lm & 1) + lr;   // matrix lm: keys 8*(lm&1) ..
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {                // 16 columns per ldmatrix.x4
+                    const uint32_t half = st + 2 * kHalfBytes + (np >> 2) * kHalfBytes;
+                    const int chunk = 2 * (np & 3) + (lm >> 1);  // columns 8*(lm>>1) ..
+                    uint32_t vb[4];
+                    ldsm_x4_trans(half + row * 128 + ((chunk ^ lr) << 4), vb);
+                    mma_bf16(o_acc[2 * np], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], vb[0], vb[1]);
+                    mma_bf16(o_acc[2 * np + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], vb[2],
+                             vb[3]);
+                }
             }
             __syncwarp();
             if (lane == 0)
@@ -291,14 +344,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     float *comb_m = reinterpret_cast<float *>(smem + L::kOffCombM);
     float *comb_l = reinterpret_cast<float *>(smem + L::kOffCombL);
     if (warp < NC) {
+        float l_tot = l_part;
+        l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+        l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+        if (g_row < G) {
+            float *dst = comb_acc + (warp * G + g_row) * kHeadDim + 2 * t4;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float l_tot = warp_sum(l_part[g]);
-            *reinterpret_cast<float4 *>(comb_acc + (warp * G + g) * kHeadDim + 4 * lane) =
-                make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-            if (lane == 0) {
-                comb_m[warp * G + g] = m_run[g];
-                comb_l[warp * G + g] = l_tot;
+            for (int n = 0; n < 16; ++n)
+                *reinterpret_cast<float2 *>(dst + 8 * n) =
+                    make_float2(o_acc[n][0] + o_acc[n][2], o_acc[n][1] + o_acc[n][3]);
+            if (t4 == 0) {
+                comb_m[warp * G + g_row] = m_run;
+                comb_l[warp * G + g_row] = l_tot;
             }
         }
     }
@@ -333,21 +390,34 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         if (c4 == 0)
             p.partial_lse[row] = (mx + log2f(den)) * kLn2;
     }
+    // This CTA's partials are written: a dependent merge grid may launch.
+    __syncthreads();
+    griddep_launch_dependents();
 }
 
-// Launch shape per group size: consumer warps, stages, resident CTAs per SM.
-template <int G> struct Shape { static constexpr int NC = 6, NS = 6, MIN_CTAS = 2; };
-template <> struct Shape<8> { static constexpr int NC = 4, NS = 4, MIN_CTAS = 2; };
+// Launch shape: consumer warps, stages, resident CTAs per SM (compile-time;
+// the defaults are the measured best on GB300).
+#ifndef FD_SPLIT_CONSUMER_WARPS
+#define FD_SPLIT_CONSUMER_WARPS 4
+#endif
+#ifndef FD_SPLIT_STAGES
+#define FD_SPLIT_STAGES 4
+#endif
+#ifndef FD_SPLIT_CTAS_PER_SM
+#define FD_SPLIT_CTAS_PER_SM 2
+#endif
+constexpr int kNC = FD_SPLIT_CONSUMER_WARPS;
+constexpr int kNS = FD_SPLIT_STAGES;
+constexpr int kMinCtas = FD_SPLIT_CTAS_PER_SM;
 
 template <int G>
 cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitParams &p,
                      int num_work, cudaStream_t stream)
 {
-    constexpr int NC = Shape<G>::NC, NS = Shape<G>::NS;
-    using L = Layout<G, NC, NS>;
-    static_assert(2 * (L::kAlloc + 1024) <= 233472 || Shape<G>::MIN_CTAS == 1,
-                  "two CTAs per SM must fit in shared memory");
-    auto kern = split_kv_kernel<G, NC, NS, Shape<G>::MIN_CTAS>;
+    using L = Layout<G, kNC, kNS>;
+    static_assert(kMinCtas * (L::kAlloc + 1024) <= 233472,
+                  "the resident CTAs must fit in shared memory");
+    auto kern = split_kv_kernel<G, kNC, kNS, kMinCtas>;
     // The shared-memory opt-in is per device; remember it for the first 64.
     static bool configured[64] = {};
     int dev = 0;
@@ -361,11 +431,16 @@ cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitPa
         if (dev < 64)
             configured[dev] = true;
     }
-    kern<<<num_work, (NC + 1) * 32, L::kAlloc, stream>>>(tk, tv, p);
+    kern<<<num_work, (kNC + 1) * 32, L::kAlloc, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+int split_ctas_per_sm()
+{
+    return kMinCtas;
+}
 
 cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
                          int group, int num_work, cudaStream_t stream)
