@@ -43,8 +43,16 @@
  *
  * Workspace: a caller-owned device buffer, zero-filled before its first use.
  * Its first FD_WORKSPACE_HEADER_BYTES hold the device status word; fd_decode
- * also keeps the split partials in it (size: fd_plan_info.workspace_bytes).
- * Calls that share one workspace must be ordered on one stream.
+ * also keeps in it one merge ticket per (request, KV head) and the split
+ * partials (size: fd_plan_info.workspace_bytes).  The tickets return to zero
+ * at the end of every successful call; after a call that reported an error
+ * status, zero the workspace again before reusing it.  Calls that share one
+ * workspace must be ordered on one stream.
+ *
+ * Launches: the kernels are launched with programmatic stream serialisation:
+ * each may begin launching while the previous grid in the stream finishes,
+ * and waits for that grid to complete before it reads or writes global
+ * memory, so stream order is kept.
  */
 #ifndef FD_H
 #define FD_H
@@ -118,13 +126,17 @@ int fd_num_sms(int device, int *num_sms);
  *
  * Article §2 (split grid = batch x heads x chunks) and §6 (chunk size tuning
  * guide: enough CTAs to fill the SMs, chunks not so small that the stage-2
- * reduction dominates).  With chunk == 0 the plan takes
- *     C = max(FD_MIN_CHUNK, roundup(ceil(T * Hkv / (num_sms * ctas_per_sm)), FD_TILE_TOKENS))
- * so the grid covers about ctas_per_sm CTAs per SM; chunk > 0 forces C (must be
- * a positive multiple of FD_TILE_TOKENS).
+ * reduction dominates, adapted to the load).  With chunk == 0 the plan tries
+ *     C_w = max(FD_MIN_CHUNK, roundup(ceil(T * Hkv / (w * num_sms * ctas_per_sm)), FD_TILE_TOKENS))
+ * for w = 1, 2, 4, 8 waves of resident CTAs, simulates how the hardware would
+ * dispatch each grid in launch order onto num_sms * ctas_per_sm slots (per-CTA
+ * cost = its 32-key tiles + a fixed overhead), and keeps the shortest.  Even
+ * batches get one wave; ragged ones get smaller chunks that balance the
+ * slots.  chunk > 0 forces C (must be a positive multiple of FD_TILE_TOKENS).
  *
  * kv_indptr_host: host int32 [batch+1].  num_sms: 0 = query the current
- * device.  ctas_per_sm: 0 = default (2).  Writes *info; returns
+ * device.  ctas_per_sm: resident CTAs per SM; 0 = what the split kernel's
+ * launch shape fits (2).  Writes *info; returns
  * FD_ERR_INVALID_ARG for a malformed indptr or head counts,
  * FD_ERR_UNSUPPORTED for an unsupported head_dim or group size.
  */
@@ -173,10 +185,14 @@ int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
 
 /*
  * fd_decode -- plan (default chunking for the current device), stage 1 and
- * stage 2 in one call; the partials live in the workspace, which must hold
- * fd_plan_info.workspace_bytes (FD_ERR_WORKSPACE otherwise; query it with
- * fd_plan for the same arguments).  Needs kv_indptr on the host (for the plan)
- * and on the device (for the kernels); the two must hold the same values.
+ * stage 2 in one call.  Stage 2 is fused into the split kernel: the CTA that
+ * finishes a (request, KV head) group last (a ticket in the workspace) merges
+ * the group's partials with the same arithmetic as fd_merge, and a request
+ * with a single split writes O and LSE directly.  The partials live in the
+ * workspace, which must hold fd_plan_info.workspace_bytes (FD_ERR_WORKSPACE
+ * otherwise; query it with fd_plan for the same arguments).  Needs kv_indptr
+ * on the host (for the plan) and on the device (for the kernels); the two must
+ * hold the same values.
  */
 int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
               const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,

@@ -128,18 +128,14 @@ extern "C" int fd_num_sms(int device, int *num_sms)
     return FD_OK;
 }
 
-extern "C" int fd_decode_split(const fd_plan_info *info, const void *q, const void *k,
-                               const void *v, const int32_t *kv_indptr_dev, float scale,
-                               float *partial_o, float *partial_lse, void *workspace,
-                               int64_t workspace_bytes, void *stream)
+namespace {
+
+// Stage 1 launch shared by fd_decode_split (partials only) and fd_decode
+// (stage 2 fused into the split kernel: o/lse/counters non-null).
+int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const void *v,
+                  const int32_t *kv_indptr_dev, float scale, float *partial_o, float *partial_lse,
+                  void *workspace, float *o, float *lse, int *counters, cudaStream_t stream)
 {
-    int rc = check_info(info);
-    if (rc != FD_OK)
-        return rc;
-    if (!workspace || workspace_bytes < FD_WORKSPACE_HEADER_BYTES)
-        return FD_ERR_WORKSPACE;
-    if (info->num_work == 0)
-        return FD_OK;
     if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
         return FD_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(partial_o, 16) ||
@@ -149,6 +145,7 @@ extern "C" int fd_decode_split(const fd_plan_info *info, const void *q, const vo
         return FD_ERR_INVALID_ARG;
 
     CUtensorMap tm_k, tm_v;
+    int rc;
     if ((rc = make_kv_map(&tm_k, k, info->total_tokens, info->num_kv_heads)) != FD_OK ||
         (rc = make_kv_map(&tm_v, v, info->total_tokens, info->num_kv_heads)) != FD_OK)
         return rc;
@@ -167,9 +164,31 @@ extern "C" int fd_decode_split(const fd_plan_info *info, const void *q, const vo
     p.total_tokens = (int32_t)info->total_tokens;
     p.q_scale = scale * 1.4426950408889634f;
     p.timeout_ns = info->timeout_ns;
+    p.fuse_merge = counters != nullptr;
+    p.o = o;
+    p.lse = lse;
+    p.counters = counters;
     const cudaError_t e =
-        fd::launch_split(tm_k, tm_v, p, info->group_size, info->num_work, as_stream(stream));
+        fd::launch_split(tm_k, tm_v, p, info->group_size, info->num_work, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int fd_decode_split(const fd_plan_info *info, const void *q, const void *k,
+                               const void *v, const int32_t *kv_indptr_dev, float scale,
+                               float *partial_o, float *partial_lse, void *workspace,
+                               int64_t workspace_bytes, void *stream)
+{
+    const int rc = check_info(info);
+    if (rc != FD_OK)
+        return rc;
+    if (!workspace || workspace_bytes < FD_WORKSPACE_HEADER_BYTES)
+        return FD_ERR_WORKSPACE;
+    if (info->num_work == 0)
+        return FD_OK;
+    return launch_stage1(info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
+                         nullptr, nullptr, nullptr, as_stream(stream));
 }
 
 extern "C" int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
@@ -199,6 +218,7 @@ extern "C" int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
     p.num_qo_heads = info->num_qo_heads;
     p.chunk = info->chunk;
     p.num_partial_rows = info->num_partial_rows;
+    p.only_empty = 0;
     const cudaError_t e = fd::launch_merge(p, as_stream(stream));
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
@@ -214,16 +234,44 @@ extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head
         return rc;
     if (!workspace || workspace_bytes < info.workspace_bytes)
         return FD_ERR_WORKSPACE;
+    if (batch == 0)
+        return FD_OK;
+    if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4) || !kv_indptr_dev)
+        return FD_ERR_INVALID_ARG;
+    // workspace: status header | tickets [B * Hkv] | partial LSE | partial O
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *partial_lse = reinterpret_cast<float *>(ws + FD_WORKSPACE_HEADER_BYTES);
-    float *partial_o = reinterpret_cast<float *>(
-        ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)info.num_partial_rows * 4, 256));
-    rc = fd_decode_split(&info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
-                         workspace_bytes, stream);
-    if (rc != FD_OK)
-        return rc;
-    return fd_merge(&info, kv_indptr_dev, partial_o, partial_lse, o, lse, workspace,
-                    workspace_bytes, stream);
+    int *counters = reinterpret_cast<int *>(ws + FD_WORKSPACE_HEADER_BYTES);
+    uint8_t *after = ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)batch * num_kv_heads * 4, 256);
+    float *partial_lse = reinterpret_cast<float *>(after);
+    float *partial_o =
+        reinterpret_cast<float *>(after + round_up((int64_t)info.num_partial_rows * 4, 256));
+    cudaStream_t s = as_stream(stream);
+    if (info.num_work > 0) {
+        rc = launch_stage1(&info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
+                           o, lse, counters, s);
+        if (rc != FD_OK)
+            return rc;
+    }
+    // Stage 2 is fused into the split kernel; only requests with no keys (no
+    // CTA of their own) still need their O = 0, LSE = -inf rows written.
+    bool any_empty = false;
+    for (int b = 0; b < batch && !any_empty; ++b)
+        any_empty = kv_indptr_host[b + 1] == kv_indptr_host[b];
+    if (!any_empty)
+        return FD_OK;
+    fd::MergeParams p;
+    p.kv_indptr = kv_indptr_dev;
+    p.partial_o = partial_o;
+    p.partial_lse = partial_lse;
+    p.o = o;
+    p.lse = lse;
+    p.status = static_cast<int *>(workspace);
+    p.batch = info.batch;
+    p.num_qo_heads = info.num_qo_heads;
+    p.chunk = info.chunk;
+    p.num_partial_rows = info.num_partial_rows;
+    p.only_empty = 1;
+    return fd::launch_merge(p, s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
 extern "C" int fd_get_device_status(void *workspace, void *stream)

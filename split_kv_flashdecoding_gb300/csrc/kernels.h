@@ -21,6 +21,13 @@ struct SplitParams {
     int32_t total_tokens;
     float q_scale;              // softmax scale * log2(e): logits are kept in base 2
     int64_t timeout_ns;
+    // Fused stage 2 (fd_decode): the last CTA of each (request, KV head) group
+    // merges the group's partials into o/lse; a request with a single split
+    // writes o/lse directly.  counters: [B * Hkv] zero-initialised tickets.
+    int32_t fuse_merge;
+    float *o;                   // [B, Hq, D]
+    float *lse;                 // [B, Hq]
+    int *counters;
 };
 
 struct MergeParams {
@@ -34,9 +41,12 @@ struct MergeParams {
     int32_t num_qo_heads;
     int32_t chunk;
     int32_t num_partial_rows;
+    int32_t only_empty;         // write only the rows of requests with no keys
 };
 
-// Stage 1: one CTA per (split, KV head); grid = num_work.
+// Stage 1: one CTA per (split, KV head); grid = num_work.  Launched as a
+// programmatic dependent of the preceding grid (it waits for that grid before
+// touching global memory).
 cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
                          int group, int num_work, cudaStream_t stream);
 

@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
         return;
     const int n = s_info[1];
     float *o_row = p.o + (int64_t)blockIdx.x * kHeadDim;
+    if (p.only_empty && n > 0)
+        return;
     if (n == 0) {   // a request with no keys
         if (warp == 0) {
             reinterpret_cast<float4 *>(o_row)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);

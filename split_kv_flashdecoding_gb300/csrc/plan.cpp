@@ -7,6 +7,11 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
+#include <map>
+#include <utility>
+#include <vector>
+
 #include "fd.h"
 #include "plan_rule.h"
 
@@ -24,6 +29,116 @@ bool supported_group(int g)
 int64_t round_up(int64_t x, int64_t m)
 {
     return (x + m - 1) / m * m;
+}
+
+// Fixed cost of one CTA (launch, pipeline fill, epilogue), in units of the
+// time one 32-key tile takes per resident CTA.
+constexpr int64_t kCtaOverheadTiles = 3;
+
+int64_t chunk_for_target(int64_t total, int num_kv_heads, int64_t target)
+{
+    int64_t c = round_up((total * num_kv_heads + target - 1) / target, FD_TILE_TOKENS);
+    if (c < FD_MIN_CHUNK)
+        c = FD_MIN_CHUNK;
+    if (c > (1 << 30))
+        c = 1 << 30;
+    return c;
+}
+
+struct GridCost {
+    int64_t ctas;          // CTAs of the grid
+    int64_t total;         // sum of CTA costs
+    int64_t largest;       // largest CTA cost
+};
+
+GridCost grid_cost(int batch, const int32_t *indptr, int num_kv_heads, int32_t c)
+{
+    GridCost g{0, 0, 0};
+    for (int b = 0; b < batch; ++b) {
+        const int32_t len = indptr[b + 1] - indptr[b];
+        const int32_t n = fd::splits_for(len, c);
+        if (n == 0)
+            continue;
+        const int32_t split_len = fd::split_len_for(len, n);
+        const int32_t tail = len - (n - 1) * split_len;
+        const int64_t full_cost = (split_len + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS + kCtaOverheadTiles;
+        const int64_t tail_cost = (tail + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS + kCtaOverheadTiles;
+        g.ctas += (int64_t)n * num_kv_heads;
+        g.total += ((int64_t)(n - 1) * full_cost + tail_cost) * num_kv_heads;
+        g.largest = std::max(g.largest, std::max(n > 1 ? full_cost : 0, tail_cost));
+    }
+    return g;
+}
+
+// Makespan, in tile units, of the split grid for chunk c: CTAs in launch order
+// (request by request, split by split, KV head fastest) go to the earliest free
+// of `slots` resident-CTA slots, as the hardware block scheduler does.  The
+// slots are kept as (free time -> count), so a run of equal CTAs costs a few
+// map operations.
+int64_t simulate_makespan(int batch, const int32_t *indptr, int num_kv_heads, int32_t c,
+                          int64_t slots)
+{
+    std::map<int64_t, int64_t> free_at{{0, slots}};
+    std::vector<std::pair<int64_t, int64_t>> taken;
+    for (int b = 0; b < batch; ++b) {
+        const int32_t len = indptr[b + 1] - indptr[b];
+        const int32_t n = fd::splits_for(len, c);
+        if (n == 0)
+            continue;
+        const int32_t split_len = fd::split_len_for(len, n);
+        for (int32_t s = 0; s < n; ++s) {
+            const int32_t keys = std::min(split_len, len - s * split_len);
+            const int64_t cost = (keys + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS + kCtaOverheadTiles;
+            int64_t need = num_kv_heads;   // the KV heads of one split, in a row
+            taken.clear();
+            while (need > 0) {
+                auto it = free_at.begin();
+                const int64_t k = std::min(need, it->second);
+                taken.emplace_back(it->first + cost, k);
+                need -= k;
+                if ((it->second -= k) == 0)
+                    free_at.erase(it);
+            }
+            for (const auto &t : taken)
+                free_at[t.first] += t.second;
+        }
+    }
+    return free_at.rbegin()->first;
+}
+
+// Choose the chunk length: for each candidate grid of about 1, 2, 4 or 8
+// waves of resident CTAs, estimate the makespan and keep the shortest (the
+// fewest waves on a tie).  A grid that fits the slots takes as long as its
+// largest CTA; otherwise the dispatch is simulated, unless the lower bound
+// total / slots already rules the candidate out.  One wave is best when the
+// requests split evenly; ragged batches gain from smaller chunks that even
+// out the per-slot load.
+int64_t choose_chunk(int batch, const int32_t *indptr, int num_kv_heads, int64_t slots)
+{
+    const int64_t total = indptr[batch];
+    int64_t best_c = chunk_for_target(total, num_kv_heads, slots);
+    int64_t best_t = -1, last_c = -1;
+    for (int waves : {1, 2, 4, 8}) {
+        const int64_t c = chunk_for_target(total, num_kv_heads, slots * waves);
+        if (c == last_c)
+            continue;
+        last_c = c;
+        const GridCost g = grid_cost(batch, indptr, num_kv_heads, (int32_t)c);
+        int64_t t;
+        if (g.ctas <= slots) {
+            t = g.largest;
+        } else {
+            const int64_t lower = std::max(g.largest, (g.total + slots - 1) / slots);
+            if (best_t >= 0 && lower >= best_t)
+                continue;
+            t = simulate_makespan(batch, indptr, num_kv_heads, (int32_t)c, slots);
+        }
+        if (best_t < 0 || t < best_t) {
+            best_t = t;
+            best_c = c;
+        }
+    }
+    return best_c;
 }
 
 }  // namespace
@@ -59,14 +174,8 @@ extern "C" int fd_plan(int batch, int num_qo_heads, int num_kv_heads, int head_d
 
     const int64_t total = kv_indptr_host[batch];
     int64_t c = chunk;
-    if (c == 0) {
-        const int64_t target = (int64_t)num_sms * ctas_per_sm;
-        c = round_up((total * num_kv_heads + target - 1) / target, FD_TILE_TOKENS);
-        if (c < FD_MIN_CHUNK)
-            c = FD_MIN_CHUNK;
-        if (c > (1 << 30))
-            c = 1 << 30;
-    }
+    if (c == 0)
+        c = choose_chunk(batch, kv_indptr_host, num_kv_heads, (int64_t)num_sms * ctas_per_sm);
 
     int64_t total_splits = 0;
     int32_t max_splits = 0;
@@ -95,8 +204,11 @@ extern "C" int fd_plan(int batch, int num_qo_heads, int num_kv_heads, int head_d
     info->num_sms = num_sms;
     info->ctas_per_sm = ctas_per_sm;
     info->total_tokens = total;
-    info->workspace_bytes = FD_WORKSPACE_HEADER_BYTES + round_up(rows * 4, 256) +
-                            rows * head_dim * 4;
+    // fd_decode workspace: status header, one ticket per (request, KV head),
+    // partial LSE, partial O.
+    info->workspace_bytes = FD_WORKSPACE_HEADER_BYTES +
+                            round_up((int64_t)batch * num_kv_heads * 4, 256) +
+                            round_up(rows * 4, 256) + rows * head_dim * 4;
     info->timeout_ns = FD_DEFAULT_TIMEOUT_NS;
     return FD_OK;
 }

@@ -47,7 +47,7 @@ constexpr int kHalfBytes = kTile * 128;        // 32 keys x 64 bf16 (one swizzle
 constexpr int kStageBytes = 4 * kHalfBytes;    // K lo, K hi, V lo, V hi
 constexpr int kMaxGroup = 8;                   // rows 8-15 of the MMA carry the lo part of P
 
-enum Misc { kB, kPrefix, kSplits, kS, kT0, kT1, kOk, kAbort, kIssued, kMiscCount };
+enum Misc { kB, kPrefix, kSplits, kS, kT0, kT1, kOk, kAbort, kIssued, kLast, kMiscCount };
 
 template <int G, int NC, int NS>
 struct Layout {
@@ -100,6 +100,68 @@ __device__ __forceinline__ float bf16_round(float x)
     return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// Stage 2 for one (request, KV head) group, run by the CTA that finished the
+// group last: for each of its G heads, M = max_i LSE_i, w_i = exp(LSE_i - M),
+// O = sum_i w_i O_i / sum_i w_i, LSE = M + ln sum_i w_i over the group's splits
+// (running maximum over batches of 8 rows, as in the merge kernel).  The
+// partials of the other CTAs are read through L2 (ld.global.cg).
+template <int G, int NTHREADS>
+__device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, int splits, int b,
+                                            int kvh, int tid)
+{
+    constexpr int kBatch = 8;
+    for (int idx = tid; idx < G * 32; idx += NTHREADS) {
+        const int g = idx >> 5, c4 = idx & 31;
+        const int hq = kvh * G + g;
+        const int64_t base = partial_row(prefix, p.num_qo_heads, hq, splits, 0);
+        const float *lse_in = p.partial_lse + base;
+        const float4 *o_in = reinterpret_cast<const float4 *>(p.partial_o + base * kHeadDim) + c4;
+        float m = -INFINITY, den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < splits; s0 += kBatch) {
+            float l[kBatch];
+            float4 v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (s0 + u < splits) {
+                    l[u] = __ldcg(lse_in + s0 + u);
+                    v[u] = __ldcg(o_in + (int64_t)(s0 + u) * (kHeadDim / 4));
+                } else {
+                    l[u] = -INFINITY;
+                    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            float bm = l[0];
+#pragma unroll
+            for (int u = 1; u < kBatch; ++u)
+                bm = fmaxf(bm, l[u]);
+            const float m_new = fmaxf(m, bm);
+            const float f = expf(m - m_new);
+            den *= f;
+            acc.x *= f;
+            acc.y *= f;
+            acc.z *= f;
+            acc.w *= f;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const float w = expf(l[u] - m_new);
+                den += w;
+                acc.x = fmaf(w, v[u].x, acc.x);
+                acc.y = fmaf(w, v[u].y, acc.y);
+                acc.z = fmaf(w, v[u].z, acc.z);
+                acc.w = fmaf(w, v[u].w, acc.w);
+            }
+            m = m_new;
+        }
+        const float inv = 1.f / den;
+        const int64_t row = (int64_t)b * p.num_qo_heads + hq;
+        reinterpret_cast<float4 *>(p.o + row * kHeadDim)[c4] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (c4 == 0)
+            p.lse[row] = m + logf(den);
+    }
+}
+
 template <int G, int NC, int NS, int MIN_CTAS>
 __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     split_kv_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -115,6 +177,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kvh = blockIdx.x % p.num_kv_heads;
     const int32_t j = blockIdx.x / p.num_kv_heads;
+    // The inputs may come from the preceding grid in the stream: wait for it
+    // before touching global memory (the launch itself overlaps its tail).
+    griddep_wait();
 
     // ---- the producer warp locates this CTA's split (same rule as the host
     // planner), sets up the barriers and puts the first NS tiles in flight
@@ -362,6 +427,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     __syncthreads();
 
     const int prefix = misc[kPrefix], splits = misc[kSplits], split = misc[kS];
+    // A request with one split needs no stage 2 when it is fused: write O/LSE.
+    const bool direct = p.fuse_merge && splits == 1;
     for (int idx = tid; idx < G * 32; idx += (NC + 1) * 32) {
         const int g = idx >> 5, c4 = idx & 31;
         float mx = -INFINITY;
@@ -385,12 +452,41 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         o.y *= inv;
         o.z *= inv;
         o.w *= inv;
-        const int64_t row = partial_row(prefix, p.num_qo_heads, kvh * G + g, splits, split);
-        *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + 4 * c4) = o;
-        if (c4 == 0)
-            p.partial_lse[row] = (mx + log2f(den)) * kLn2;
+        const float lse_nat = (mx + log2f(den)) * kLn2;
+        if (direct) {
+            const int64_t row = (int64_t)b * p.num_qo_heads + kvh * G + g;
+            *reinterpret_cast<float4 *>(p.o + row * kHeadDim + 4 * c4) = o;
+            if (c4 == 0)
+                p.lse[row] = lse_nat;
+        } else {
+            const int64_t row = partial_row(prefix, p.num_qo_heads, kvh * G + g, splits, split);
+            *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + 4 * c4) = o;
+            if (c4 == 0)
+                p.partial_lse[row] = lse_nat;
+        }
     }
-    // This CTA's partials are written: a dependent merge grid may launch.
+
+    if (p.fuse_merge && splits > 1) {
+        // Ticket: the last CTA of the (request, KV head) group to finish merges
+        // the group (stage 2).  Fence before the ticket so this CTA's partials
+        // are visible to whichever CTA merges; the last one resets the ticket.
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            int *cnt = p.counters + (int64_t)b * p.num_kv_heads + kvh;
+            const int prev = atomicAdd(cnt, 1);
+            const bool last = prev == splits - 1;
+            if (last)
+                atomicExch(cnt, 0);
+            misc[kLast] = last;
+        }
+        __syncthreads();
+        if (misc[kLast]) {
+            __threadfence();
+            merge_group<G, (NC + 1) * 32>(p, prefix, splits, b, kvh, tid);
+        }
+    }
+    // This CTA's outputs are written: a dependent grid may launch.
     __syncthreads();
     griddep_launch_dependents();
 }
@@ -431,8 +527,17 @@ cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitPa
         if (dev < 64)
             configured[dev] = true;
     }
-    kern<<<num_work, (kNC + 1) * 32, L::kAlloc, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_work);
+    cfg.blockDim = dim3((kNC + 1) * 32);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace

@@ -233,3 +233,55 @@ def test_device_indptr_inconsistent_with_plan_is_flagged(cuda_device):
     res = two_stage(dev, chunk=32, guard=2)
     assert fd.get_device_status(res["ws"]) == -6
     check_guards(res)
+
+
+FUSED_CASES = SMALL_CASES + [
+    ("many_splits", 1, 32, 8, [5000]),
+    ("ragged_many", 6, 16, 2, [3000, 0, 17, 900, 4100, 1]),
+    ("g8_long", 2, 64, 8, [9000, 2500]),
+]
+
+
+@pytest.mark.parametrize("name,B,Hq,Hkv,lengths", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])
+def test_fused_decode_small(cuda_device, name, B, Hq, Hkv, lengths):
+    """fd_decode (stage 2 fused into the split kernel: ticket merge, direct
+    writes for single-split requests, zero rows for empty ones), called twice
+    on one workspace with different values: the tickets reset themselves."""
+    o_refs = []
+    ws = None
+    for rep in range(2):
+        inp = make_small(B, Hq, Hkv, 128, lengths, seed=zlib.crc32(name.encode()) % 1000 + rep)
+        dev = to_device(inp, cuda_device)
+        if ws is None:
+            ws = torch.zeros(fd.workspace_bytes(B, Hq, Hkv, 128, inp["kv_indptr"]),
+                             dtype=torch.uint8, device=cuda_device)
+        o, lse = fd.decode(dev["q"], dev["k"], dev["v"], inp["kv_indptr"], dev["kv_indptr_dev"],
+                           inp["scale"], workspace=ws)
+        torch.cuda.synchronize()
+        assert fd.get_device_status(ws) == 0
+        o_ref, lse_ref = _oracle(inp)
+        err = errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
+        assert_within(err, what=f"{name} rep {rep}")
+        assert_within(err, **TIGHT, what=f"{name} rep {rep} (tight)")
+        o_refs.append(o_ref)
+    # the tickets are back to zero after each call
+    tickets = ws[256:256 + 4 * B * Hkv].view(torch.int32)
+    assert torch.all(tickets == 0)
+
+
+def test_fused_decode_after_timeout_with_rezeroed_workspace(cuda_device):
+    """After a call reports an error status, zeroing the workspace makes the
+    next fd_decode correct again (tickets and status start from zero)."""
+    inp = make_small(1, 32, 8, 128, [6000], seed=8)
+    dev = to_device(inp, cuda_device)
+    res = two_stage(dev, timeout_ns=0)
+    assert fd.get_device_status(res["ws"]) == -5
+    ws = torch.zeros(fd.workspace_bytes(1, 32, 8, 128, inp["kv_indptr"]), dtype=torch.uint8,
+                     device=cuda_device)
+    o, lse = fd.decode(dev["q"], dev["k"], dev["v"], inp["kv_indptr"], dev["kv_indptr_dev"],
+                       inp["scale"], workspace=ws)
+    torch.cuda.synchronize()
+    assert fd.get_device_status(ws) == 0
+    o_ref, lse_ref = _oracle(inp)
+    assert_within(errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape),
+                         lse_ref.reshape(lse.shape)), **TIGHT)

@@ -118,7 +118,52 @@ def test_forced_split_counts_one_to_max():
 def test_workspace_bytes():
     info = fd.plan(3, 16, 4, 128, [0, 10, 10, 300], num_sms=10, chunk=64)
     rows = info.num_partial_rows
-    assert info.workspace_bytes == 256 + -(-rows * 4 // 256) * 256 + rows * 128 * 4
+    tickets = -(-3 * 4 * 4 // 256) * 256           # one int32 per (request, KV head)
+    assert info.workspace_bytes == 256 + tickets + -(-rows * 4 // 256) * 256 + rows * 128 * 4
+
+
+def _makespan(info, ip, slots, overhead=3):
+    """Independent re-simulation of the block dispatch (heap of slot free times)."""
+    import heapq
+    items = fd.plan_work_items(info, ip)
+    heap = [0] * slots
+    end = 0
+    for _, _, _, t0, t1 in items:
+        start = heapq.heappop(heap)
+        fin = start + -(-(t1 - t0) // 32) + overhead
+        heapq.heappush(heap, fin)
+        end = max(end, fin)
+    return end
+
+
+def test_ragged_batches_get_more_waves_than_even_ones():
+    """The planner simulates the block dispatch: a batch-1 request that splits
+    evenly gets one wave of resident CTAs, a ragged batch smaller chunks that
+    balance the slots."""
+    slots = 152 * 2
+    one = fd.plan(1, 32, 8, 128, indptr_of([65536]), num_sms=152, ctas_per_sm=2)
+    assert one.num_work == slots
+    rng = np.random.default_rng(3)
+    ragged_len = rng.integers(512, 16385, size=64)
+    ragged = fd.plan(64, 32, 8, 128, indptr_of(ragged_len), num_sms=152, ctas_per_sm=2)
+    one_wave_chunk = -(-int(ragged_len.sum()) * 8 // slots)
+    assert ragged.chunk < one_wave_chunk
+    assert ragged.num_work > slots
+
+
+@pytest.mark.parametrize("lengths", [[65536], [131072], [32768] * 16, [2048], [5000, 300, 70000],
+                                     list(np.random.default_rng(5).integers(512, 16385, 64))])
+def test_chosen_chunk_is_best_of_the_candidates(lengths):
+    """The chunk the planner picks has the shortest re-simulated makespan among
+    the 1/2/4/8-wave candidates (ties go to fewer waves)."""
+    ip = indptr_of(lengths)
+    slots = 152 * 2
+    chosen = fd.plan(len(lengths), 32, 8, 128, ip, num_sms=152, ctas_per_sm=2)
+    best = _makespan(chosen, ip, slots)
+    for waves in (1, 2, 4, 8):
+        c = max(128, -(-(-(-int(ip[-1]) * 8 // (slots * waves))) // 32) * 32)
+        cand = fd.plan(len(lengths), 32, 8, 128, ip, num_sms=152, chunk=c)
+        assert best <= _makespan(cand, ip, slots)
 
 
 def test_empty_batch_and_empty_requests():
