@@ -204,8 +204,8 @@ extern "C" int fd_plan(int batch, int num_qo_heads, int num_kv_heads, int head_d
     info->num_sms = num_sms;
     info->ctas_per_sm = ctas_per_sm;
     info->total_tokens = total;
-    // fd_decode workspace: status header, one ticket per (request, KV head),
-    // partial LSE, partial O.
+    // fd_decode workspace: status header, one merge ticket per (request, KV
+    // head), partial LSE, partial O.
     info->workspace_bytes = FD_WORKSPACE_HEADER_BYTES +
                             round_up((int64_t)batch * num_kv_heads * 4, 256) +
                             round_up(rows * 4, 256) + rows * head_dim * 4;

@@ -34,6 +34,7 @@
 // loop was limited by shared-memory wavefronts (broadcast reads of q and p)
 // and instruction issue, not by HBM; the contraction itself stays tiny
 // (m = G <= 8 rows).
+#include <cuda/atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -61,6 +62,8 @@ struct Layout {
     static constexpr int kOffCombM = NC * G * kHeadDim * 4;
     static constexpr int kOffCombL = kOffCombM + NC * G * 4;
     static_assert(kOffCombL + NC * G * 4 <= NS * kStageBytes, "combine area must fit the ring");
+    // The fused stage-2 merge of the last CTA also works over the drained ring.
+    static_assert((NC + 1) * G * (kHeadDim + 2) * 4 <= NS * kStageBytes, "merge area must fit the ring");
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
@@ -102,63 +105,108 @@ __device__ __forceinline__ float bf16_round(float x)
 
 // Stage 2 for one (request, KV head) group, run by the CTA that finished the
 // group last: for each of its G heads, M = max_i LSE_i, w_i = exp(LSE_i - M),
-// O = sum_i w_i O_i / sum_i w_i, LSE = M + ln sum_i w_i over the group's splits
-// (running maximum over batches of 8 rows, as in the merge kernel).  The
-// partials of the other CTAs are read through L2 (ld.global.cg).
-template <int G, int NTHREADS>
+// O = sum_i w_i O_i / sum_i w_i, LSE = M + ln sum_i w_i over the group's splits.
+// Warp w of the NW warps takes splits w, w + NW, ... (U splits of loads in
+// flight per batch, lane = 4 output columns, all G heads), keeps a running
+// maximum per head, and the NW warp states are combined through shared memory
+// (`scratch`, free once the stage ring has drained).  The other CTAs' partials
+// are read through L2 (ld.global.cg).
+template <int G, int NW>
 __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, int splits, int b,
-                                            int kvh, int tid)
+                                            int kvh, int warp, int lane, float *scratch)
 {
-    constexpr int kBatch = 8;
-    for (int idx = tid; idx < G * 32; idx += NTHREADS) {
-        const int g = idx >> 5, c4 = idx & 31;
-        const int hq = kvh * G + g;
-        const int64_t base = partial_row(prefix, p.num_qo_heads, hq, splits, 0);
-        const float *lse_in = p.partial_lse + base;
-        const float4 *o_in = reinterpret_cast<const float4 *>(p.partial_o + base * kHeadDim) + c4;
-        float m = -INFINITY, den = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < splits; s0 += kBatch) {
-            float l[kBatch];
-            float4 v[kBatch];
+    constexpr int U = (16 / G) > 1 ? 16 / G : 1;   // splits per batch: 16 float4 in flight
+    float m[G], den[G];
+    float4 acc[G];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                if (s0 + u < splits) {
-                    l[u] = __ldcg(lse_in + s0 + u);
-                    v[u] = __ldcg(o_in + (int64_t)(s0 + u) * (kHeadDim / 4));
+    for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        den[g] = 0.f;
+        acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int64_t row0 = partial_row(prefix, p.num_qo_heads, kvh * G, splits, 0);
+    for (int s0 = warp; s0 < splits; s0 += NW * U) {
+        float l[U][G];
+        float4 v[U][G];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + u * NW;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                // rows of head kvh*G + g are splits apart
+                const int64_t row = row0 + (int64_t)g * splits + s;
+                if (s < splits) {
+                    l[u][g] = __ldcg(p.partial_lse + row);
+                    v[u][g] = __ldcg(reinterpret_cast<const float4 *>(p.partial_o + row * kHeadDim) + lane);
                 } else {
-                    l[u] = -INFINITY;
-                    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    l[u][g] = -INFINITY;
+                    v[u][g] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-            float bm = l[0];
-#pragma unroll
-            for (int u = 1; u < kBatch; ++u)
-                bm = fmaxf(bm, l[u]);
-            const float m_new = fmaxf(m, bm);
-            const float f = expf(m - m_new);
-            den *= f;
-            acc.x *= f;
-            acc.y *= f;
-            acc.z *= f;
-            acc.w *= f;
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const float w = expf(l[u] - m_new);
-                den += w;
-                acc.x = fmaf(w, v[u].x, acc.x);
-                acc.y = fmaf(w, v[u].y, acc.y);
-                acc.z = fmaf(w, v[u].z, acc.z);
-                acc.w = fmaf(w, v[u].w, acc.w);
-            }
-            m = m_new;
         }
-        const float inv = 1.f / den;
-        const int64_t row = (int64_t)b * p.num_qo_heads + hq;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float bm = l[0][g];
+#pragma unroll
+            for (int u = 1; u < U; ++u)
+                bm = fmaxf(bm, l[u][g]);
+            const float m_new = fmaxf(m[g], bm);
+            if (m_new == -INFINITY)   // only empty partials so far (none in practice)
+                continue;
+            const float f = expf(m[g] - m_new);
+            den[g] *= f;
+            acc[g].x *= f;
+            acc[g].y *= f;
+            acc[g].z *= f;
+            acc[g].w *= f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float w = expf(l[u][g] - m_new);
+                den[g] += w;
+                acc[g].x = fmaf(w, v[u][g].x, acc[g].x);
+                acc[g].y = fmaf(w, v[u][g].y, acc[g].y);
+                acc[g].z = fmaf(w, v[u][g].z, acc[g].z);
+                acc[g].w = fmaf(w, v[u][g].w, acc[g].w);
+            }
+            m[g] = m_new;
+        }
+    }
+    float *s_acc = scratch;                       // [NW][G][128]
+    float *s_m = scratch + NW * G * kHeadDim;     // [NW][G]
+    float *s_den = s_m + NW * G;                  // [NW][G]
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        reinterpret_cast<float4 *>(s_acc + (warp * G + g) * kHeadDim)[lane] = acc[g];
+        if (lane == 0) {
+            s_m[warp * G + g] = m[g];
+            s_den[warp * G + g] = den[g];
+        }
+    }
+    __syncthreads();
+    for (int idx = warp * 32 + lane; idx < G * 32; idx += NW * 32) {
+        const int g = idx >> 5, c4 = idx & 31;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            mx = fmaxf(mx, s_m[w * G + g]);
+        float d = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = expf(s_m[w * G + g] - mx);   // 0 for a warp with no splits
+            d = fmaf(f, s_den[w * G + g], d);
+            const float4 t = reinterpret_cast<const float4 *>(s_acc + (w * G + g) * kHeadDim)[c4];
+            a.x = fmaf(f, t.x, a.x);
+            a.y = fmaf(f, t.y, a.y);
+            a.z = fmaf(f, t.z, a.z);
+            a.w = fmaf(f, t.w, a.w);
+        }
+        const float inv = 1.f / d;
+        const int64_t row = (int64_t)b * p.num_qo_heads + kvh * G + g;
         reinterpret_cast<float4 *>(p.o + row * kHeadDim)[c4] =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
         if (c4 == 0)
-            p.lse[row] = m + logf(den);
+            p.lse[row] = mx + logf(d);
     }
 }
 
@@ -439,7 +487,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < NC; ++w) {
-            const float e = exp2f(comb_m[w * G + g] - mx);
+            const float e = mx == -INFINITY ? 0.f : exp2f(comb_m[w * G + g] - mx);
             den = fmaf(e, comb_l[w * G + g], den);
             const float4 a = *reinterpret_cast<const float4 *>(comb_acc + (w * G + g) * kHeadDim + 4 * c4);
             o.x = fmaf(e, a.x, o.x);
@@ -447,12 +495,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
             o.z = fmaf(e, a.z, o.z);
             o.w = fmaf(e, a.w, o.w);
         }
-        const float inv = 1.f / den;
+        const float inv = den > 0.f ? 1.f / den : 0.f;
         o.x *= inv;
         o.y *= inv;
         o.z *= inv;
         o.w *= inv;
-        const float lse_nat = (mx + log2f(den)) * kLn2;
+        const float lse_nat = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
         if (direct) {
             const int64_t row = (int64_t)b * p.num_qo_heads + kvh * G + g;
             *reinterpret_cast<float4 *>(p.o + row * kHeadDim + 4 * c4) = o;
@@ -468,23 +516,24 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
 
     if (p.fuse_merge && splits > 1) {
         // Ticket: the last CTA of the (request, KV head) group to finish merges
-        // the group (stage 2).  Fence before the ticket so this CTA's partials
-        // are visible to whichever CTA merges; the last one resets the ticket.
+        // the group (stage 2).  The ticket add is acquire-release at GPU scope:
+        // it publishes this CTA's partials (made visible to thread 0 by the
+        // barrier) and lets the last CTA see everyone else's; that CTA also
+        // resets the ticket for the next call.
         __syncthreads();
         if (tid == 0) {
-            __threadfence();
-            int *cnt = p.counters + (int64_t)b * p.num_kv_heads + kvh;
-            const int prev = atomicAdd(cnt, 1);
+            cuda::atomic_ref<int, cuda::thread_scope_device> ticket(
+                p.counters[(int64_t)b * p.num_kv_heads + kvh]);
+            const int prev = ticket.fetch_add(1, cuda::memory_order_acq_rel);
             const bool last = prev == splits - 1;
             if (last)
-                atomicExch(cnt, 0);
+                ticket.store(0, cuda::memory_order_relaxed);
             misc[kLast] = last;
         }
         __syncthreads();
-        if (misc[kLast]) {
-            __threadfence();
-            merge_group<G, (NC + 1) * 32>(p, prefix, splits, b, kvh, tid);
-        }
+        if (misc[kLast])
+            merge_group<G, NC + 1>(p, prefix, splits, b, kvh, warp, lane,
+                                   reinterpret_cast<float *>(smem));
     }
     // This CTA's outputs are written: a dependent grid may launch.
     __syncthreads();

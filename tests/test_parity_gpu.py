@@ -264,9 +264,8 @@ def test_fused_decode_small(cuda_device, name, B, Hq, Hkv, lengths):
         assert_within(err, what=f"{name} rep {rep}")
         assert_within(err, **TIGHT, what=f"{name} rep {rep} (tight)")
         o_refs.append(o_ref)
-    # the tickets are back to zero after each call
-    tickets = ws[256:256 + 4 * B * Hkv].view(torch.int32)
-    assert torch.all(tickets == 0)
+    # the merge tickets are back to zero after each call
+    assert torch.all(ws[256:256 + 4 * B * Hkv].view(torch.int32) == 0)
 
 
 def test_fused_decode_after_timeout_with_rezeroed_workspace(cuda_device):

@@ -118,8 +118,9 @@ def test_forced_split_counts_one_to_max():
 def test_workspace_bytes():
     info = fd.plan(3, 16, 4, 128, [0, 10, 10, 300], num_sms=10, chunk=64)
     rows = info.num_partial_rows
-    tickets = -(-3 * 4 * 4 // 256) * 256           # one int32 per (request, KV head)
-    assert info.workspace_bytes == 256 + tickets + -(-rows * 4 // 256) * 256 + rows * 128 * 4
+    group = -(-3 * 4 * 4 // 256) * 256             # one int32 per (request, KV head)
+    # header | merge tickets | partial LSE | partial O
+    assert info.workspace_bytes == 256 + group + -(-rows * 4 // 256) * 256 + rows * 128 * 4
 
 
 def _makespan(info, ip, slots, overhead=3):
