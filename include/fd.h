@@ -201,6 +201,38 @@ int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
               void *stream);
 
 /*
+ * fd_decode_static_workspace -- fd_decode for callers that cannot allocate.
+ *
+ * The article has no counterpart: this is a library convenience.  Some
+ * callers run decode attention where they must not allocate device memory:
+ * the enqueue step of an inference-engine plugin, a runtime whose memory is
+ * planned up front and owned by someone else, code that may not grow the
+ * process's footprint.  This entry point needs only the inputs and outputs.
+ * Its scratch (status word, merge tickets, split partials) is a fixed device
+ * array of FD_STATIC_WORKSPACE_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits; it calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Arguments and results as fd_decode, without the workspace.  Returns
+ * FD_ERR_WORKSPACE, before touching the GPU, when the plan for these
+ * arguments needs more than FD_STATIC_WORKSPACE_BYTES (fd_plan reports the
+ * need in fd_plan_info.workspace_bytes); use fd_decode with a workspace then.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Each call
+ * clears the status word and the merge tickets on its stream before it runs.
+ * All calls share the one array, which keeps the last call's contents: calls
+ * that can overlap on the GPU (other streams, other host threads, without
+ * ordering between them) race and give wrong results.  The status word is
+ * not reachable from outside the library, so errors the kernels detect are
+ * not reported by this entry point.
+ */
+#define FD_STATIC_WORKSPACE_BYTES (16 << 20)
+int fd_decode_static_workspace(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                               const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+                               const void *q, const void *k, const void *v, float scale,
+                               float *o, float *lse, void *stream);
+
+/*
  * fd_get_device_status -- synchronise the stream, read and clear the status
  * word the kernels write into the workspace.  Returns FD_OK,
  * FD_ERR_TIMEOUT, FD_ERR_DEVICE_BOUNDS, or FD_ERR_CUDA if the read failed.

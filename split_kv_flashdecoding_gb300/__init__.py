@@ -10,6 +10,8 @@ Entry points (same names as the C ABI, minus the ``fd_`` prefix):
   decode_split(...)                     stage 1: partial (O_i, LSE_i) per split
   merge(...)                            stage 2: LSE merge into O, LSE
   decode(...)        -> (O, LSE)        plan + stage 1 + stage 2
+  decode_static_workspace(...)          the same for callers that cannot allocate
+                                        (scratch in a fixed array in the library)
   get_device_status(workspace)          read and clear the kernels' error word
 
 There is no CPU fallback: if libfd.so cannot be loaded, importing the library
@@ -82,6 +84,7 @@ SIGNATURES = {
     "fd_merge": ([_PI, _P, _P, _P, _P, _P, _P, _I64, _P], _I),
     "fd_decode": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
     "fd_get_device_status": ([_P, _P], _I),
+    "fd_decode_static_workspace": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _P, _P, _P], _I),
 }
 
 
@@ -214,6 +217,29 @@ def decode(q, k, v, kv_indptr_host, kv_indptr_dev, scale: float, *, o=None, lse=
     return o, lse
 
 
+def decode_static_workspace(q, k, v, kv_indptr_host, kv_indptr_dev, scale: float, *, o=None,
+                            lse=None, stream=None):
+    """fd_decode_static_workspace: fd_decode for callers that cannot allocate.
+
+    The library keeps the scratch in a fixed device array (16 MiB per GPU), so
+    only inputs and outputs are passed; o/lse are allocated here only when not
+    given.  Calls that can overlap on the GPU race (they share the array).
+    """
+    import torch
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    ip = _host_indptr(kv_indptr_host)
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().fd_decode_static_workspace(B, Hq, Hkv, D, ip.ctypes.data_as(ctypes.c_void_p),
+                                            _ptr(kv_indptr_dev), _ptr(q), _ptr(k), _ptr(v),
+                                            float(scale), _ptr(o), _ptr(lse), _stream(stream)),
+           "fd_decode_static_workspace")
+    return o, lse
+
+
 def get_device_status(workspace, stream=None) -> int:
     """fd_get_device_status: synchronise, read and clear the kernels' status word."""
     return lib().fd_get_device_status(_ptr(workspace), _stream(stream))
@@ -221,6 +247,7 @@ def get_device_status(workspace, stream=None) -> int:
 
 __all__ = [
     "PlanInfo", "FdError", "lib", "build", "plan", "plan_work_items", "decode_split", "merge",
-    "decode", "get_device_status", "workspace_bytes", "num_sms", "status_string",
+    "decode", "decode_static_workspace", "get_device_status", "workspace_bytes", "num_sms",
+    "status_string",
     "TILE_TOKENS", "WORKSPACE_HEADER_BYTES", "DEFAULT_TIMEOUT_NS",
 ]
