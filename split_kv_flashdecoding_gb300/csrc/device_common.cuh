@@ -183,9 +183,9 @@ __device__ __forceinline__ bool derive_split(const int32_t *__restrict__ kv_indp
     for (int base = 0; base < batch; base += 32) {
         const int b = base + lane;
         int32_t beg = 0, end = 0, n = 0;
-        if (b < batch) {
-            beg = __ldg(kv_indptr + b);
-            end = __ldg(kv_indptr + b + 1);
+        if (b < batch) {   // plain loads: kv_indptr may point into global or parameter space
+            beg = kv_indptr[b];
+            end = kv_indptr[b + 1];
             n = splits_for(end - beg, chunk);
         }
         int32_t incl = n;

@@ -134,7 +134,8 @@ namespace {
 // (stage 2 fused into the split kernel: o/lse/counters non-null).
 int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const void *v,
                   const int32_t *kv_indptr_dev, float scale, float *partial_o, float *partial_lse,
-                  void *workspace, float *o, float *lse, int *counters, cudaStream_t stream)
+                  void *workspace, float *o, float *lse, int *counters,
+                  const int32_t *kv_indptr_host, cudaStream_t stream)
 {
     if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
         return FD_ERR_INVALID_ARG;
@@ -168,6 +169,12 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.o = o;
     p.lse = lse;
     p.counters = counters;
+    // kv_indptr_host is only known on the fd_decode path (the same values as
+    // the device copy, by contract).
+    p.indptr_in_params = kv_indptr_host && info->batch + 1 <= fd::kParamIndptr;
+    memset(p.indptr_param, 0, sizeof p.indptr_param);
+    if (p.indptr_in_params)
+        memcpy(p.indptr_param, kv_indptr_host, (size_t)(info->batch + 1) * sizeof(int32_t));
     const cudaError_t e =
         fd::launch_split(tm_k, tm_v, p, info->group_size, info->num_work, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
@@ -188,7 +195,7 @@ extern "C" int fd_decode_split(const fd_plan_info *info, const void *q, const vo
     if (info->num_work == 0)
         return FD_OK;
     return launch_stage1(info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
-                         nullptr, nullptr, nullptr, as_stream(stream));
+                         nullptr, nullptr, nullptr, nullptr, as_stream(stream));
 }
 
 extern "C" int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
@@ -248,7 +255,7 @@ extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head
     cudaStream_t s = as_stream(stream);
     if (info.num_work > 0) {
         rc = launch_stage1(&info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
-                           o, lse, counters, s);
+                           o, lse, counters, kv_indptr_host, s);
         if (rc != FD_OK)
             return rc;
     }

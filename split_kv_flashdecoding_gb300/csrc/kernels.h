@@ -7,6 +7,10 @@
 
 namespace fd {
 
+// Small batches carry kv_indptr in the launch parameters as well, so a CTA
+// finds its key range without a dependent global load before its first copy.
+constexpr int kParamIndptr = 33;   // batch <= 32
+
 struct SplitParams {
     const uint16_t *q;          // bf16 [B, Hq, D]
     const int32_t *kv_indptr;   // device [B+1]
@@ -28,6 +32,8 @@ struct SplitParams {
     float *o;                   // [B, Hq, D]
     float *lse;                 // [B, Hq]
     int *counters;
+    int32_t indptr_in_params;   // 1: indptr_param holds kv_indptr[0..batch]
+    int32_t indptr_param[kParamIndptr];
 };
 
 struct MergeParams {

@@ -213,7 +213,8 @@ __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, in
 template <int G, int NC, int NS, int MIN_CTAS>
 __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     split_kv_kernel(const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const SplitParams p)
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ SplitParams p)
 {
     using L = Layout<G, NC, NS>;
     extern __shared__ uint8_t smem_raw[];
@@ -227,7 +228,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     const int32_t j = blockIdx.x / p.num_kv_heads;
     // The inputs may come from the preceding grid in the stream: wait for it
     // before touching global memory (the launch itself overlaps its tail).
-    griddep_wait();
+    // When kv_indptr is in the launch parameters, the producer warp locates
+    // its split before that wait.
+    const bool early_derive = p.indptr_in_params && warp == NC;
+    if (!early_derive)
+        griddep_wait();
 
     // ---- the producer warp locates this CTA's split (same rule as the host
     // planner), sets up the barriers and puts the first NS tiles in flight
@@ -237,7 +242,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     int issued = 0;
     if (warp == NC) {
         SplitCoord c{};
-        bool ok = derive_split(p.kv_indptr, p.batch, p.chunk, j, false, c);
+        bool ok = derive_split(p.indptr_in_params ? p.indptr_param : p.kv_indptr, p.batch,
+                               p.chunk, j, false, c);
+        if (early_derive)
+            griddep_wait();
         if (lane == 0) {
             int32_t t0 = 0, t1 = 0;
             if (ok) {
