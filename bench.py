@@ -205,7 +205,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     import torch
 
     import split_kv_flashdecoding_gb300 as fd
-    from workloads import make_inputs
+    from workloads import make_inputs, to_paged
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -225,10 +225,23 @@ def run_fd(args, world, rank, local) -> dict | None:
     # small workloads rotate through enough copies of their inputs.
     kv_bytes = 2 * T * Hkv * D * 2
     copies = max(1, -(-2 * L2_BYTES // max(kv_bytes, 1)))
-    bufs = [tuple(inp[x].to(dev) for x in ("q", "k", "v")) for _ in range(copies)]
+    paged = args.page_size > 0
+    if paged:   # the same keys in a paged KV cache (scattered pages)
+        pg = to_paged(inp, args.page_size, seed=13)
+        bufs = [tuple(pg[x].to(dev) for x in ("q", "k_pages", "v_pages")) for _ in range(copies)]
+        pg_ip = np.ascontiguousarray(pg["kv_page_indptr"].numpy().astype(np.int32))
+        pg_last = np.ascontiguousarray(pg["kv_last_page_len"].numpy().astype(np.int32))
+        pg_ip_dev = pg["kv_page_indptr"].to(dev)
+        pg_last_dev = pg["kv_last_page_len"].to(dev)
+        pg_idx_dev = pg["kv_page_indices"].to(dev)
+        num_pages = pg["k_pages"].shape[0]
+        del pg
+    else:
+        bufs = [tuple(inp[x].to(dev) for x in ("q", "k", "v")) for _ in range(copies)]
     q, k, v = bufs[0]
 
-    info0 = fd.plan(B, Hq, Hkv, D, ip_host)
+    info0 = (fd.plan_paged(B, Hq, Hkv, D, args.page_size, pg_ip, pg_last) if paged
+             else fd.plan(B, Hq, Hkv, D, ip_host))
     rows = info0.num_partial_rows
     nb = step_bytes(B, Hq, Hkv, D, T, rows)
     ws_split = torch.zeros(fd.WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=dev)
@@ -244,20 +257,30 @@ def run_fd(args, world, rank, local) -> dict | None:
     sp = P(stream.cuda_stream)
     ipp = ip_host.ctypes.data_as(P)
 
-    # One step = fd_decode through the C ABI: host plan + split kernel + merge
-    # kernel.  Arguments are marshalled once so the host stays ahead of the GPU.
-    step_args = [(B, Hq, Hkv, D, ipp, P(ip_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()),
-                  P(vc.data_ptr()), ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()),
-                  P(ws.data_ptr()), ws.numel(), sp) for qc, kc, vc in bufs]
+    # One step = fd_decode (or fd_decode_paged) through the C ABI: host plan +
+    # the split kernel, which also runs stage 2 in the last CTA of each group.
+    # Arguments are marshalled once so the host stays ahead of the GPU.
+    if paged:
+        step_args = [(B, Hq, Hkv, D, args.page_size, num_pages, pg_ip.ctypes.data_as(P),
+                      pg_last.ctypes.data_as(P), P(pg_ip_dev.data_ptr()), P(pg_last_dev.data_ptr()),
+                      P(pg_idx_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()),
+                      ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()), P(ws.data_ptr()),
+                      ws.numel(), sp) for qc, kc, vc in bufs]
+        step_fn, step_name = lib.fd_decode_paged, "fd_decode_paged"
+    else:
+        step_args = [(B, Hq, Hkv, D, ipp, P(ip_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()),
+                      P(vc.data_ptr()), ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()),
+                      P(ws.data_ptr()), ws.numel(), sp) for qc, kc, vc in bufs]
+        step_fn, step_name = lib.fd_decode, "fd_decode"
     split_args = [(ctypes.byref(info0), P(qc.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()),
                    P(ip_dev.data_ptr()), ctypes.c_float(scale), P(po.data_ptr()),
                    P(pl.data_ptr()), P(ws_split.data_ptr()), ws_split.numel(), sp)
                   for qc, kc, vc in bufs]
 
     def step(i):
-        rc = lib.fd_decode(*step_args[i % copies])
+        rc = step_fn(*step_args[i % copies])
         if rc != 0:
-            raise fd.FdError(rc, "fd_decode")
+            raise fd.FdError(rc, step_name)
 
     for i in range(args.warmup):
         step(i)
@@ -280,23 +303,30 @@ def run_fd(args, world, rank, local) -> dict | None:
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
         barrier(world)
-    launches = K * (2 if info0.num_work > 0 else 1)
+    # stage 2 runs inside the split kernel; the merge kernel is launched only
+    # when some request has no keys
+    any_empty = bool(np.any(np.diff(ip_host) == 0))
+    launches = K * (int(info0.num_work > 0) + int(any_empty))
     status = fd.get_device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {fd.status_string(status)}")
     ms = max_over_ranks(ev0.elapsed_time(ev1) / K, world, dev)
 
     # The dominant kernel alone (stage 1), back to back on the same stream.
-    n_split = min(K, 500)
-    torch.cuda._sleep(2_000_000)
-    ev0.record(stream)
-    for i in range(n_split):
-        rc = lib.fd_decode_split(*split_args[i % copies])
-        if rc != 0:
-            raise fd.FdError(rc, "fd_decode_split")
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    split_avg = ev0.elapsed_time(ev1) / n_split
+    # A paged step has no separate stage-1 entry point: its one kernel is the step.
+    if paged:
+        split_avg = ms
+    else:
+        n_split = min(K, 500)
+        torch.cuda._sleep(2_000_000)
+        ev0.record(stream)
+        for i in range(n_split):
+            rc = lib.fd_decode_split(*split_args[i % copies])
+            if rc != 0:
+                raise fd.FdError(rc, "fd_decode_split")
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        split_avg = ev0.elapsed_time(ev1) / n_split
 
     # The same step timed one at a time after an L2 flush (includes each
     # step's launch latency and about 2 us of event overhead).
@@ -314,7 +344,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, fd_decode, D2H of O and LSE, all inside the events
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not paged:
         q_h, k_h, v_h = (inp[x].pin_memory() for x in ("q", "k", "v"))
         ip_h = inp["kv_indptr"].pin_memory()
         o_h = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
@@ -348,8 +378,9 @@ def run_fd(args, world, rank, local) -> dict | None:
     if rank != 0:
         return None
     peak, peak_kind = measured_peaks()
-    achieved = nb["split"] / (split_avg * 1e-3) / 1e9
-    traffic = profiled_traffic(w.name)
+    kernel_bytes = nb["step"] if paged else nb["split"]
+    achieved = kernel_bytes / (split_avg * 1e-3) / 1e9
+    traffic = None if paged else profiled_traffic(w.name)
     gbs = aggregate_gbs(nb["step"], world, ms)
     line = {
         "metric": METRIC,
@@ -377,11 +408,13 @@ def run_fd(args, world, rank, local) -> dict | None:
                    "step_us_after_l2_flush_p10_p50_p90": [
                        round(float(np.percentile(flushed_ms, p)) * 1e3, 2) for p in (10, 50, 90)],
                    "wall_s": round(t_wall, 3),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "kv_layout": (f"paged, page_size {args.page_size}, pages scattered in a pool"
+                                 if paged else "ragged packed")},
         "roofline": {"bound": "hbm", "kernel": "split_kv_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "algorithmic_bytes_per_launch": nb["split"],
+                     "algorithmic_bytes_per_launch": kernel_bytes,
                      "traffic": traffic},
         "gpu_launches": launches,
         "clocks": clocks.summary(),
@@ -479,6 +512,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[x.name for x in WORKLOADS])
     ap.add_argument("--impl", default="fd", choices=["fd", "reference"])
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="time fd_decode_paged on the same keys laid out as a paged KV cache")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

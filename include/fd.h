@@ -201,6 +201,49 @@ int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
               void *stream);
 
 /*
+ * Paged KV cache -- FD++ §6 ("vLLM and TensorRT-LLM integration"): the engine
+ * keeps K/V in fixed-size physical pages from a page table, and each split
+ * chunk streams the pages its keys fall in.
+ *
+ * Layout:
+ *     k_pages, v_pages      bf16  [num_pages, page_size, Hkv, D]   page pools
+ *     kv_page_indptr        int32 [B+1]   request b owns page-list entries
+ *                                          kv_page_indptr[b] .. kv_page_indptr[b+1]-1
+ *     kv_page_indices       int32 [kv_page_indptr[B]]   physical page of each entry
+ *     kv_last_page_len      int32 [B]     keys in request b's last page, 1..page_size
+ * Request b's keys are, in order, rows 0..page_size-1 of its pages, the last
+ * page filled to kv_last_page_len[b]; it has (pages_b - 1) * page_size +
+ * kv_last_page_len[b] keys (0 with no pages).  page_size must be a positive
+ * multiple of 16 (FD_ERR_UNSUPPORTED otherwise).  A page index outside
+ * [0, num_pages) sets FD_ERR_DEVICE_BOUNDS in the status word (the page is not
+ * read).
+ */
+
+/*
+ * fd_plan_paged -- fd_plan for a paged layout: the same chunking on the
+ * requests' key counts (host only).  Sizes the fd_decode_paged workspace.
+ */
+int fd_plan_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                  const int32_t *kv_page_indptr_host, const int32_t *kv_last_page_len_host,
+                  int num_sms, int ctas_per_sm, int chunk, fd_plan_info *info);
+
+/*
+ * fd_decode_paged -- fd_decode over a paged KV cache: plan, stage 1 with each
+ * 32-key tile copied from the page it lies in (TMA boxes never cross a page),
+ * stage 2 fused.  kv_page_indptr and kv_last_page_len are given on the host
+ * (for the plan) and on the device (for the kernels) with the same values;
+ * kv_page_indices on the device.  Workspace as fd_decode, sized by
+ * fd_plan_paged.
+ */
+int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                    int num_pages, const int32_t *kv_page_indptr_host,
+                    const int32_t *kv_last_page_len_host, const int32_t *kv_page_indptr_dev,
+                    const int32_t *kv_last_page_len_dev, const int32_t *kv_page_indices_dev,
+                    const void *q, const void *k_pages, const void *v_pages, float scale,
+                    float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                    void *stream);
+
+/*
  * fd_decode_static_workspace -- fd_decode for callers that cannot allocate.
  *
  * The article has no counterpart: this is a library convenience.  Some

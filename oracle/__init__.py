@@ -11,6 +11,9 @@ two-stage global reduction".
   split_partials(...)     §3 stage 1: per-chunk (acc, local max m, local sum l)
   normalised(acc, m, l)   the same partial as (O_i, LSE_i) = (acc/l, m + ln l)
   merge(acc, m, l, seg)   §3 stage 2: rescale by exp(m_i - M) and reduce
+  gather_paged(...)       a paged KV cache read through its page table into the
+                          ragged layout decode() takes (§6: the engine's page
+                          table maps each request's keys onto physical pages)
 
 The arithmetic is in fd_oracle.c (fp64 throughout); this module only
 marshals arrays.  build() compiles it with gcc.
@@ -182,3 +185,32 @@ def merge(acc, m, l, seg_indptr):
     if rc != 0:
         raise ValueError("fdo_merge rejected its arguments")
     return o, lse
+
+
+def gather_paged(k_pages, v_pages, kv_page_indptr, kv_page_indices, kv_last_page_len):
+    """Read a paged KV cache through its page table (plain indexing).
+
+    Request b's keys are rows 0..page_size-1 of pages
+    kv_page_indices[kv_page_indptr[b]:kv_page_indptr[b+1]] in that order, the
+    last page holding kv_last_page_len[b] keys.  Returns (K, V, kv_indptr) in
+    the ragged layout: K/V [T, Hkv, D] (same dtype), kv_indptr int64 [B+1].
+    """
+    import torch
+    ip = [int(x) for x in np.asarray(kv_page_indptr).reshape(-1)]
+    idx = [int(x) for x in np.asarray(kv_page_indices).reshape(-1)]
+    last = [int(x) for x in np.asarray(kv_last_page_len).reshape(-1)]
+    ks, vs, lens = [], [], []
+    for b in range(len(ip) - 1):
+        L = 0
+        for j in range(ip[b], ip[b + 1]):
+            n = last[b] if j == ip[b + 1] - 1 else k_pages.shape[1]
+            ks.append(k_pages[idx[j], :n])
+            vs.append(v_pages[idx[j], :n])
+            L += n
+        lens.append(L)
+    indptr = np.zeros(len(lens) + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(lens)
+    if ks:
+        return torch.cat(ks), torch.cat(vs), indptr
+    shape = (0, k_pages.shape[2], k_pages.shape[3])
+    return torch.zeros(shape, dtype=k_pages.dtype), torch.zeros(shape, dtype=v_pages.dtype), indptr

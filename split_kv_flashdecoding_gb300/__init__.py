@@ -12,6 +12,7 @@ Entry points (same names as the C ABI, minus the ``fd_`` prefix):
   decode(...)        -> (O, LSE)        plan + stage 1 + stage 2
   decode_static_workspace(...)          the same for callers that cannot allocate
                                         (scratch in a fixed array in the library)
+  plan_paged(...), decode_paged(...)    the same over a paged KV cache (page tables)
   get_device_status(workspace)          read and clear the kernels' error word
 
 There is no CPU fallback: if libfd.so cannot be loaded, importing the library
@@ -85,6 +86,9 @@ SIGNATURES = {
     "fd_decode": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
     "fd_get_device_status": ([_P, _P], _I),
     "fd_decode_static_workspace": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _P, _P, _P], _I),
+    "fd_plan_paged": ([_I, _I, _I, _I, _I, _P, _P, _I, _I, _I, _PI], _I),
+    "fd_decode_paged": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P,
+                         _P, _I64, _P], _I),
 }
 
 
@@ -240,6 +244,51 @@ def decode_static_workspace(q, k, v, kv_indptr_host, kv_indptr_dev, scale: float
     return o, lse
 
 
+def plan_paged(batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+               kv_page_indptr_host, kv_last_page_len_host, *, num_sms: int = 0,
+               ctas_per_sm: int = 0, chunk: int = 0) -> PlanInfo:
+    """fd_plan_paged: the plan of a paged layout (host only)."""
+    ip = _host_indptr(kv_page_indptr_host)
+    ll = _host_indptr(kv_last_page_len_host)
+    if ip.size != batch + 1 or ll.size != batch:
+        raise FdError(-1, "kv_page_indptr must have batch+1 and kv_last_page_len batch entries")
+    info = PlanInfo()
+    _check(lib().fd_plan_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                               ip.ctypes.data_as(ctypes.c_void_p), ll.ctypes.data_as(ctypes.c_void_p),
+                               num_sms, ctas_per_sm, chunk, ctypes.byref(info)), "fd_plan_paged")
+    return info
+
+
+def decode_paged(q, k_pages, v_pages, kv_page_indptr_host, kv_last_page_len_host,
+                 kv_page_indptr_dev, kv_last_page_len_dev, kv_page_indices_dev, scale: float, *,
+                 o=None, lse=None, workspace=None, stream=None):
+    """fd_decode_paged: q [B,Hq,D], page pools k/v [num_pages, page_size, Hkv, D] bf16.
+
+    Page tables as in include/fd.h (host copies of indptr and last-page
+    lengths for the plan, device copies plus the page indices for the kernels).
+    """
+    import torch
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    ip = _host_indptr(kv_page_indptr_host)
+    ll = _host_indptr(kv_last_page_len_host)
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = plan_paged(B, Hq, Hkv, D, page_size, ip, ll).workspace_bytes
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    _check(lib().fd_decode_paged(B, Hq, Hkv, D, page_size, num_pages,
+                                 ip.ctypes.data_as(ctypes.c_void_p),
+                                 ll.ctypes.data_as(ctypes.c_void_p), _ptr(kv_page_indptr_dev),
+                                 _ptr(kv_last_page_len_dev), _ptr(kv_page_indices_dev), _ptr(q),
+                                 _ptr(k_pages), _ptr(v_pages), float(scale), _ptr(o), _ptr(lse),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)), "fd_decode_paged")
+    return o, lse
+
+
 def get_device_status(workspace, stream=None) -> int:
     """fd_get_device_status: synchronise, read and clear the kernels' status word."""
     return lib().fd_get_device_status(_ptr(workspace), _stream(stream))
@@ -247,7 +296,8 @@ def get_device_status(workspace, stream=None) -> int:
 
 __all__ = [
     "PlanInfo", "FdError", "lib", "build", "plan", "plan_work_items", "decode_split", "merge",
-    "decode", "decode_static_workspace", "get_device_status", "workspace_bytes", "num_sms",
+    "decode", "decode_static_workspace", "plan_paged", "decode_paged", "get_device_status",
+    "workspace_bytes", "num_sms",
     "status_string",
     "TILE_TOKENS", "WORKSPACE_HEADER_BYTES", "DEFAULT_TIMEOUT_NS",
 ]

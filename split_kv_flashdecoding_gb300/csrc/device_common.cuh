@@ -120,6 +120,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 3-D tiled TMA load of box (x, y, z) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                            int32_t y, int32_t z, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch
 
 // Allow the next grid in the stream (launched with programmatic stream
@@ -163,30 +174,58 @@ __device__ __forceinline__ float warp_sum(float x)
 
 // ------------------------------------------------------- split derivation
 
+// Where each request's keys live.
+//   ragged: indptr = key-row prefix [B+1]; request b's keys are the rows
+//           indptr[b] .. indptr[b+1]-1 of K/V [T, Hkv, D].
+//   paged:  indptr = page-list prefix [B+1]; request b's keys fill, in order,
+//           the pages page_indices[indptr[b] .. indptr[b+1]-1] of the page pool
+//           [num_pages, page_size, Hkv, D], the last one up to last_len[b] keys.
+struct KeyIndex {
+    const int32_t *indptr;
+    const int32_t *last_len;   // null: ragged
+    int32_t page_size;
+
+    // base: first key row (ragged) or first page-list entry (paged); len: keys;
+    // pages: page-list entries (paged) or 0.
+    __device__ __forceinline__ void at(int b, int32_t &base, int32_t &len, int32_t &pages) const
+    {
+        // plain loads: the arrays may live in global or in parameter space
+        const int32_t a = indptr[b], e = indptr[b + 1];
+        base = a;
+        if (!last_len) {
+            len = e - a;
+            pages = 0;
+        } else {
+            pages = e - a;
+            len = pages > 0 ? (pages - 1) * page_size + last_len[b] : 0;
+        }
+    }
+};
+
 struct SplitCoord {
     int32_t b;        // request
     int32_t prefix;   // splits of requests before b
     int32_t splits;   // splits_b
     int32_t s;        // split within the request (when derived from a split index)
-    int32_t beg, end; // the request's key rows
+    int32_t base;     // first key row (ragged) or first page-list entry (paged)
+    int32_t len;      // keys of the request
+    int32_t pages;    // page-list entries of the request (paged)
 };
 
 // Warp-collective: locate global split `j` (if by_request is false) or request
-// `j` (if true) by scanning kv_indptr.  All lanes return the same result;
-// returns false if j is out of range.
-__device__ __forceinline__ bool derive_split(const int32_t *__restrict__ kv_indptr, int batch,
-                                             int32_t chunk, int32_t j, bool by_request,
-                                             SplitCoord &out)
+// `j` (if true) by scanning the requests' key counts.  All lanes return the
+// same result; returns false if j is out of range.
+__device__ __forceinline__ bool derive_split(const KeyIndex &ki, int batch, int32_t chunk, int32_t j,
+                                             bool by_request, SplitCoord &out)
 {
     const int lane = threadIdx.x & 31;
     int32_t carry = 0;
-    for (int base = 0; base < batch; base += 32) {
-        const int b = base + lane;
-        int32_t beg = 0, end = 0, n = 0;
-        if (b < batch) {   // plain loads: kv_indptr may point into global or parameter space
-            beg = kv_indptr[b];
-            end = kv_indptr[b + 1];
-            n = splits_for(end - beg, chunk);
+    for (int b0 = 0; b0 < batch; b0 += 32) {
+        const int b = b0 + lane;
+        int32_t base = 0, len = 0, pages = 0, n = 0;
+        if (b < batch) {
+            ki.at(b, base, len, pages);
+            n = len > 0 ? splits_for(len, chunk) : 0;
         }
         int32_t incl = n;
 #pragma unroll
@@ -204,8 +243,9 @@ __device__ __forceinline__ bool derive_split(const int32_t *__restrict__ kv_indp
             out.b = __shfl_sync(0xffffffffu, b, src);
             out.prefix = __shfl_sync(0xffffffffu, excl, src);
             out.splits = __shfl_sync(0xffffffffu, n, src);
-            out.beg = __shfl_sync(0xffffffffu, beg, src);
-            out.end = __shfl_sync(0xffffffffu, end, src);
+            out.base = __shfl_sync(0xffffffffu, base, src);
+            out.len = __shfl_sync(0xffffffffu, len, src);
+            out.pages = __shfl_sync(0xffffffffu, pages, src);
             out.s = by_request ? 0 : j - out.prefix;
             return true;
         }

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "fd.h"
 #include "kernels.h"
@@ -43,21 +44,43 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// K or V [T, Hkv, 128] bf16 seen as a 2-D tensor of T rows x Hkv*128 columns;
-// one box = 32 rows x 64 columns, 128-byte swizzle, zero fill past row T.
-int make_kv_map(CUtensorMap *map, const void *base, int64_t total_tokens, int num_kv_heads)
+// K or V [rows, Hkv, 128] bf16 (rows = T keys, or num_pages * page_size for a
+// page pool), 128-byte swizzle, zero fill past the last row.
+//  box_rows == 32: a 3-D map (64 columns, rows, Hkv * 2 column blocks of 64)
+//    whose box (64, 32, 2) brings both 64-column halves of one head's 32 rows
+//    in one copy, laid out in shared memory as [half][row][64].  The block
+//    dimension is last with a 128-byte stride, smaller than the row stride:
+//    TMA takes any 16-byte-multiple strides.
+//  box_rows == 16: a 2-D map of rows x Hkv*128 columns, box 16 rows x 64
+//    columns (one copy per half; the two halves of a 16-row box are not
+//    adjacent in the [half][32 rows][64] stage layout).
+int make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int num_kv_heads,
+                int box_rows = kBoxRows)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
         return FD_ERR_CUDA;
-    const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * kHeadDim, (cuuint64_t)total_tokens};
-    const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * kHeadDim * 2};
-    const cuuint32_t box[2] = {kBoxCols, kBoxRows};
-    const cuuint32_t elem_strides[2] = {1, 1};
-    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
-                              dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t row_stride = (cuuint64_t)num_kv_heads * kHeadDim * 2;
+    CUresult r;
+    if (box_rows == kBoxRows) {
+        const cuuint64_t dims[3] = {kBoxCols, (cuuint64_t)rows, (cuuint64_t)num_kv_heads * 2};
+        const cuuint64_t strides[2] = {row_stride, kBoxCols * 2};
+        const cuuint32_t box[3] = {kBoxCols, (cuuint32_t)box_rows, 2};
+        const cuuint32_t elem_strides[3] = {1, 1, 1};
+        r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * kHeadDim, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {row_stride};
+        const cuuint32_t box[2] = {kBoxCols, (cuuint32_t)box_rows};
+        const cuuint32_t elem_strides[2] = {1, 1};
+        r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                   strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
 }
 
@@ -130,12 +153,26 @@ extern "C" int fd_num_sms(int device, int *num_sms)
 
 namespace {
 
-// Stage 1 launch shared by fd_decode_split (partials only) and fd_decode
-// (stage 2 fused into the split kernel: o/lse/counters non-null).
+// The page-pool description of a paged KV cache (see fd_decode_paged).
+struct PagedKV {
+    int32_t page_size;
+    int32_t num_pages;
+    const int32_t *last_len_dev;
+    const int32_t *last_len_host;
+    const int32_t *page_indices_dev;
+    int32_t num_page_entries;   // kv_page_indptr[batch]
+};
+
+// Stage 1 launch shared by fd_decode_split (partials only), fd_decode and
+// fd_decode_paged (stage 2 fused into the split kernel: o/lse/counters
+// non-null).  kv_indptr_* is the key-row prefix, or the page-list prefix when
+// `paged` is given.
+
 int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const void *v,
                   const int32_t *kv_indptr_dev, float scale, float *partial_o, float *partial_lse,
                   void *workspace, float *o, float *lse, int *counters,
-                  const int32_t *kv_indptr_host, cudaStream_t stream)
+                  const int32_t *kv_indptr_host, cudaStream_t stream,
+                  const PagedKV *paged = nullptr)
 {
     if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
         return FD_ERR_INVALID_ARG;
@@ -147,8 +184,10 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
 
     CUtensorMap tm_k, tm_v;
     int rc;
-    if ((rc = make_kv_map(&tm_k, k, info->total_tokens, info->num_kv_heads)) != FD_OK ||
-        (rc = make_kv_map(&tm_v, v, info->total_tokens, info->num_kv_heads)) != FD_OK)
+    const int64_t rows = paged ? (int64_t)paged->num_pages * paged->page_size : info->total_tokens;
+    const int box_rows = paged && paged->page_size % kBoxRows != 0 ? 16 : kBoxRows;
+    if ((rc = make_kv_map(&tm_k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+        (rc = make_kv_map(&tm_v, v, rows, info->num_kv_heads, box_rows)) != FD_OK)
         return rc;
 
     fd::SplitParams p;
@@ -171,10 +210,20 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.counters = counters;
     // kv_indptr_host is only known on the fd_decode path (the same values as
     // the device copy, by contract).
-    p.indptr_in_params = kv_indptr_host && info->batch + 1 <= fd::kParamIndptr;
+    p.indptr_in_params = kv_indptr_host && info->batch + 1 <= fd::kParamIndptr &&
+                         (!paged || paged->last_len_host);
     memset(p.indptr_param, 0, sizeof p.indptr_param);
+    memset(p.last_len_param, 0, sizeof p.last_len_param);
     if (p.indptr_in_params)
         memcpy(p.indptr_param, kv_indptr_host, (size_t)(info->batch + 1) * sizeof(int32_t));
+    p.kv_last_len = paged ? paged->last_len_dev : nullptr;
+    p.page_indices = paged ? paged->page_indices_dev : nullptr;
+    p.page_size = paged ? paged->page_size : 0;
+    p.box_rows = box_rows;
+    p.num_pages = paged ? paged->num_pages : 0;
+    p.num_page_entries = paged ? paged->num_page_entries : 0;
+    if (paged && p.indptr_in_params)
+        memcpy(p.last_len_param, paged->last_len_host, (size_t)info->batch * sizeof(int32_t));
     const cudaError_t e =
         fd::launch_split(tm_k, tm_v, p, info->group_size, info->num_work, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
@@ -226,6 +275,8 @@ extern "C" int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
     p.chunk = info->chunk;
     p.num_partial_rows = info->num_partial_rows;
     p.only_empty = 0;
+    p.kv_last_len = nullptr;
+    p.page_size = 0;
     const cudaError_t e = fd::launch_merge(p, as_stream(stream));
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
@@ -278,6 +329,114 @@ extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head
     p.chunk = info.chunk;
     p.num_partial_rows = info.num_partial_rows;
     p.only_empty = 1;
+    p.kv_last_len = nullptr;
+    p.page_size = 0;
+    return fd::launch_merge(p, s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+namespace {
+
+// Host checks of a paged layout; fills the logical key-row prefix (keys of
+// request b = (pages_b - 1) * page_size + last_len_b) for the planner.
+int paged_logical_indptr(int batch, int page_size, const int32_t *page_indptr,
+                         const int32_t *last_len, std::vector<int32_t> &indptr)
+{
+    if (batch < 0 || !page_indptr || (batch > 0 && !last_len))
+        return FD_ERR_INVALID_ARG;
+    if (page_size <= 0 || page_size % 16 != 0)
+        return FD_ERR_UNSUPPORTED;
+    if (page_indptr[0] != 0)
+        return FD_ERR_INVALID_ARG;
+    indptr.assign((size_t)batch + 1, 0);
+    int64_t total = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int32_t pages = page_indptr[b + 1] - page_indptr[b];
+        if (pages < 0)
+            return FD_ERR_INVALID_ARG;
+        if (pages > 0 && (last_len[b] < 1 || last_len[b] > page_size))
+            return FD_ERR_INVALID_ARG;
+        total += pages > 0 ? (int64_t)(pages - 1) * page_size + last_len[b] : 0;
+        if (total > INT32_MAX)
+            return FD_ERR_INVALID_ARG;
+        indptr[b + 1] = (int32_t)total;
+    }
+    return FD_OK;
+}
+
+}  // namespace
+
+extern "C" int fd_plan_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                             int page_size, const int32_t *kv_page_indptr_host,
+                             const int32_t *kv_last_page_len_host, int num_sms, int ctas_per_sm,
+                             int chunk, fd_plan_info *info)
+{
+    std::vector<int32_t> indptr;
+    const int rc = paged_logical_indptr(batch, page_size, kv_page_indptr_host,
+                                        kv_last_page_len_host, indptr);
+    if (rc != FD_OK)
+        return rc;
+    return fd_plan(batch, num_qo_heads, num_kv_heads, head_dim, indptr.data(), num_sms,
+                   ctas_per_sm, chunk, info);
+}
+
+extern "C" int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                               int page_size, int num_pages, const int32_t *kv_page_indptr_host,
+                               const int32_t *kv_last_page_len_host,
+                               const int32_t *kv_page_indptr_dev,
+                               const int32_t *kv_last_page_len_dev,
+                               const int32_t *kv_page_indices_dev, const void *q,
+                               const void *k_pages, const void *v_pages, float scale, float *o,
+                               float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    fd_plan_info info;
+    int rc = fd_plan_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                           kv_page_indptr_host, kv_last_page_len_host, 0, 0, 0, &info);
+    if (rc != FD_OK)
+        return rc;
+    if (!workspace || workspace_bytes < info.workspace_bytes)
+        return FD_ERR_WORKSPACE;
+    if (batch == 0)
+        return FD_OK;
+    if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4) || !kv_page_indptr_dev ||
+        !kv_last_page_len_dev || !aligned(kv_last_page_len_dev, 4) ||
+        (info.num_work > 0 && (!kv_page_indices_dev || !aligned(kv_page_indices_dev, 4))))
+        return FD_ERR_INVALID_ARG;
+    if (num_pages <= 0 || (int64_t)num_pages * page_size > INT32_MAX)
+        return FD_ERR_INVALID_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int *counters = reinterpret_cast<int *>(ws + FD_WORKSPACE_HEADER_BYTES);
+    uint8_t *after = ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)batch * num_kv_heads * 4, 256);
+    float *partial_lse = reinterpret_cast<float *>(after);
+    float *partial_o =
+        reinterpret_cast<float *>(after + round_up((int64_t)info.num_partial_rows * 4, 256));
+    cudaStream_t s = as_stream(stream);
+    if (info.num_work > 0) {
+        const PagedKV pk{page_size, num_pages, kv_last_page_len_dev, kv_last_page_len_host,
+                         kv_page_indices_dev, kv_page_indptr_host[batch]};
+        rc = launch_stage1(&info, q, k_pages, v_pages, kv_page_indptr_dev, scale, partial_o,
+                           partial_lse, workspace, o, lse, counters, kv_page_indptr_host, s, &pk);
+        if (rc != FD_OK)
+            return rc;
+    }
+    bool any_empty = false;
+    for (int b = 0; b < batch && !any_empty; ++b)
+        any_empty = kv_page_indptr_host[b + 1] == kv_page_indptr_host[b];
+    if (!any_empty)
+        return FD_OK;
+    fd::MergeParams p;
+    p.kv_indptr = kv_page_indptr_dev;
+    p.partial_o = partial_o;
+    p.partial_lse = partial_lse;
+    p.o = o;
+    p.lse = lse;
+    p.status = static_cast<int *>(workspace);
+    p.batch = info.batch;
+    p.num_qo_heads = info.num_qo_heads;
+    p.chunk = info.chunk;
+    p.num_partial_rows = info.num_partial_rows;
+    p.only_empty = 1;
+    p.kv_last_len = kv_last_page_len_dev;
+    p.page_size = page_size;
     return fd::launch_merge(p, s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 

@@ -13,7 +13,7 @@ constexpr int kParamIndptr = 33;   // batch <= 32
 
 struct SplitParams {
     const uint16_t *q;          // bf16 [B, Hq, D]
-    const int32_t *kv_indptr;   // device [B+1]
+    const int32_t *kv_indptr;   // device [B+1]: key-row prefix (ragged) or page-list prefix (paged)
     float *partial_o;           // [rows, D]
     float *partial_lse;         // [rows]
     int *status;                // workspace status word
@@ -32,8 +32,17 @@ struct SplitParams {
     float *o;                   // [B, Hq, D]
     float *lse;                 // [B, Hq]
     int *counters;
-    int32_t indptr_in_params;   // 1: indptr_param holds kv_indptr[0..batch]
+    int32_t indptr_in_params;   // 1: indptr_param (and last_len_param) hold the device arrays
     int32_t indptr_param[kParamIndptr];
+    // Paged KV (kv_last_len non-null): K/V are page pools [num_pages, page_size,
+    // Hkv, D]; request b's pages are page_indices[kv_indptr[b] .. kv_indptr[b+1]).
+    const int32_t *kv_last_len; // [B] valid keys in each request's last page
+    const int32_t *page_indices;
+    int32_t page_size;
+    int32_t box_rows;           // rows per TMA box: 32, or 16 when pages are 16-row aligned only
+    int32_t num_pages;
+    int32_t num_page_entries;   // kv_indptr[B]
+    int32_t last_len_param[kParamIndptr];
 };
 
 struct MergeParams {
@@ -48,6 +57,8 @@ struct MergeParams {
     int32_t chunk;
     int32_t num_partial_rows;
     int32_t only_empty;         // write only the rows of requests with no keys
+    const int32_t *kv_last_len; // paged layout (see SplitParams), or null
+    int32_t page_size;
 };
 
 // Stage 1: one CTA per (split, KV head); grid = num_work.  Launched as a

@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 
     if (warp == 0) {
         SplitCoord c{};
-        const bool found = derive_split(p.kv_indptr, p.batch, p.chunk, b, true, c);
+        const KeyIndex ki{p.kv_indptr, p.kv_last_len, p.page_size};
+        const bool found = derive_split(ki, p.batch, p.chunk, b, true, c);
         if (lane == 0) {
             const bool ok = found && (c.splits == 0 ||
                                       partial_row(c.prefix, p.num_qo_heads, p.num_qo_heads - 1,

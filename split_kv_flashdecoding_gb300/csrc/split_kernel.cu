@@ -11,9 +11,11 @@
 // from HBM once per step.
 //
 // Warp roles:
-//   warp NC (producer): one lane issues 2-D TMA loads of 32-key tiles of K and
-//     V (each tile = two 64-column boxes per tensor, 128-byte swizzle) into an
-//     NS-stage ring guarded by full/empty mbarriers.
+//   warp NC (producer): one lane issues TMA loads of 32-key tiles of K and V
+//     into an NS-stage ring guarded by full/empty mbarriers.  A tile is one
+//     3-D box per tensor holding both 64-column halves of the head (128-byte
+//     swizzle), or, for a paged cache with 16-key pages, two 2-D boxes of 16
+//     rows per half.
 //   warps 0..NC-1 (consumers): warp w takes tiles w, w+NC, ...  NS is a
 //     multiple of NC, so every stage always goes to the same warp and a warp
 //     never waits on a barrier more than one phase ahead (parity waits can only
@@ -210,7 +212,7 @@ __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, in
     }
 }
 
-template <int G, int NC, int NS, int MIN_CTAS>
+template <int G, int NC, int NS, int MIN_CTAS, bool PAGED>
 __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     split_kv_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -237,25 +239,113 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     // ---- the producer warp locates this CTA's split (same rule as the host
     // planner), sets up the barriers and puts the first NS tiles in flight
     // before the block synchronises, so the loads start as early as possible.
+    // With the paged layout the whole warp runs the issue loop (it shares a
+    // window of page ids); lane 0 issues the barrier operations and the
+    // copies.  The ragged layout needs lane 0 alone.  Key positions t0, t1 are
+    // relative to the request's first key.
     const int32_t x_col = kvh * kHeadDim;
+    constexpr bool paged = PAGED;
     uint64_t pol = 0;
     int issued = 0;
+    int32_t t0 = 0, t1 = 0, req_base = 0, req_len = 0, req_pages = 0;
+    // paged: lane l holds the page id of page win_first + l, and nxt_id that
+    // of page win_first + 32 + l, loaded one window ahead so that moving on to
+    // the next window never waits for a global load.  The window starts far
+    // below page 0 so the first lookup always fills it.
+    int32_t win_first = -(1 << 30), win_id = 0, nxt_id = 0;
+    auto fetch_ids = [&](int32_t first) -> int32_t {
+        return first + lane < req_pages ? __ldg(p.page_indices + req_base + first + lane) : 0;
+    };
+
+    // Warp-collective: physical page of the request's page `pg` (paged layout).
+    auto page_id = [&](int32_t pg) -> int32_t {
+        if (pg < win_first || pg >= win_first + 32) {
+            win_id = pg == win_first + 32 ? nxt_id : fetch_ids(pg);
+            win_first = pg;
+            nxt_id = fetch_ids(pg + 32);
+        }
+        int32_t id = __shfl_sync(0xffffffffu, win_id, pg - win_first);
+        if (id < 0 || id >= p.num_pages) {   // a page outside the pool
+            if (lane == 0)
+                report(p.status, FD_ERR_DEVICE_BOUNDS);
+            id = 0;
+        }
+        return id;
+    };
+    // paged: the next box starts at row cur_off of the request's page cur_pg.
+    // Tiles are issued in order, so the cursor only moves forward.
+    int32_t cur_pg = 0, cur_off = 0;
+    auto next_box_row = [&]() -> int32_t {
+        // Rows past the request's last key read whatever its last page holds
+        // there; the consumers mask them.
+        const int32_t y = page_id(min(cur_pg, req_pages - 1)) * p.page_size + cur_off;
+        cur_off += p.box_rows;
+        if (cur_off >= p.page_size) {
+            cur_off -= p.page_size;
+            ++cur_pg;
+        }
+        return y;
+    };
+    // First rows (in K/V, or in the page pool) of tile i's boxes: ya, and yb
+    // for the second 16-row box of a paged tile.  Warp-collective for the
+    // paged layout.  The producer computes these before it waits for the
+    // tile's stage, so that only the copies remain once the stage is free.
+    auto tile_rows = [&](int i, int32_t &ya, int32_t &yb) {
+        if constexpr (!paged) {
+            ya = req_base + t0 + i * kTile;
+        } else {
+            ya = next_box_row();
+            if (p.box_rows < kTile)
+                yb = next_box_row();
+        }
+    };
+    // Lane 0: put tile i into stage i % NS.  Whole-tile boxes use the 3-D maps
+    // (both 64-column halves in one box); 16-row boxes use 2-D maps, one per
+    // half, the second box 16 rows further into the stage.
+    auto issue_tile = [&](int i, int32_t ya, int32_t yb) {
+        const int s = i % NS;
+        const uint32_t full = smem_addr(&bars[s]);
+        const uint32_t dst = smem_addr(smem + s * kStageBytes);
+        mbar_arrive_expect_tx(full, kStageBytes);
+        if (!paged || p.box_rows == kTile) {
+            tma_load_3d(dst, &tm_k, 0, ya, 2 * kvh, full, pol);
+            tma_load_3d(dst + 2 * kHalfBytes, &tm_v, 0, ya, 2 * kvh, full, pol);
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int32_t y = h ? yb : ya;
+                const uint32_t off = h * (kTile / 2) * 128;
+                tma_load_2d(dst + off, &tm_k, x_col, y, full, pol);
+                tma_load_2d(dst + kHalfBytes + off, &tm_k, x_col + 64, y, full, pol);
+                tma_load_2d(dst + 2 * kHalfBytes + off, &tm_v, x_col, y, full, pol);
+                tma_load_2d(dst + 3 * kHalfBytes + off, &tm_v, x_col + 64, y, full, pol);
+            }
+        }
+    };
+
     if (warp == NC) {
+        const KeyIndex ki = p.indptr_in_params
+                                ? KeyIndex{p.indptr_param, paged ? p.last_len_param : nullptr,
+                                           p.page_size}
+                                : KeyIndex{p.kv_indptr, p.kv_last_len, p.page_size};
         SplitCoord c{};
-        bool ok = derive_split(p.indptr_in_params ? p.indptr_param : p.kv_indptr, p.batch,
-                               p.chunk, j, false, c);
+        bool ok = derive_split(ki, p.batch, p.chunk, j, false, c);
         if (early_derive)
             griddep_wait();
+        if (ok) {
+            const int32_t len = split_len_for(c.len, c.splits);
+            t0 = c.s * len;
+            t1 = min(t0 + len, c.len);
+            req_base = c.base;
+            req_len = c.len;
+            req_pages = c.pages;
+            ok = t0 < t1 && c.base >= 0 &&
+                 (paged ? c.base + c.pages <= p.num_page_entries
+                        : c.base + c.len <= p.total_tokens) &&
+                 partial_row(c.prefix, p.num_qo_heads, p.num_qo_heads - 1, c.splits,
+                             c.splits - 1) < p.num_partial_rows;
+        }
         if (lane == 0) {
-            int32_t t0 = 0, t1 = 0;
-            if (ok) {
-                const int32_t len = split_len_for(c.end - c.beg, c.splits);
-                t0 = c.beg + c.s * len;
-                t1 = min(t0 + len, c.end);
-                ok = t0 < t1 && t1 <= p.total_tokens &&
-                     partial_row(c.prefix, p.num_qo_heads, p.num_qo_heads - 1, c.splits,
-                                 c.splits - 1) < p.num_partial_rows;
-            }
             misc[kB] = c.b;
             misc[kPrefix] = c.prefix;
             misc[kSplits] = c.splits;
@@ -269,29 +359,35 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                 mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: consumer warp releases
             }
             fence_mbar_init();
-            if (!ok) {
+            if (!ok)
                 report(p.status, FD_ERR_DEVICE_BOUNDS);
-            } else {
-                pol = l2_evict_first_policy();
-                const int first = min(NS, (t1 - t0 + kTile - 1) / kTile);
-                for (; issued < first; ++issued) {
-                    const uint32_t full = smem_addr(&bars[issued]);
-                    const uint32_t dst = smem_addr(smem + issued * kStageBytes);
-                    const int32_t y = t0 + issued * kTile;
-                    mbar_arrive_expect_tx(full, kStageBytes);
-                    tma_load_2d(dst, &tm_k, x_col, y, full, pol);
-                    tma_load_2d(dst + kHalfBytes, &tm_k, x_col + 64, y, full, pol);
-                    tma_load_2d(dst + 2 * kHalfBytes, &tm_v, x_col, y, full, pol);
-                    tma_load_2d(dst + 3 * kHalfBytes, &tm_v, x_col + 64, y, full, pol);
-                }
-            }
-            misc[kIssued] = issued;
         }
+        __syncwarp();
+        if (ok && (paged || lane == 0)) {
+            pol = l2_evict_first_policy();
+            if constexpr (paged) {
+                cur_pg = t0 / p.page_size;
+                cur_off = t0 % p.page_size;
+            }
+            const int first = min(NS, (t1 - t0 + kTile - 1) / kTile);
+            for (; issued < first; ++issued) {
+                int32_t ya = 0, yb = 0;
+                tile_rows(issued, ya, yb);
+                if (lane == 0)
+                    issue_tile(issued, ya, yb);
+            }
+        }
+        if (lane == 0)
+            misc[kIssued] = issued;
     }
+    (void)req_len;
     __syncthreads();
     if (!misc[kOk])
         return;
-    const int32_t t0 = misc[kT0], t1 = misc[kT1];
+    if (warp != NC) {
+        t0 = misc[kT0];
+        t1 = misc[kT1];
+    }
     const int n_tiles = (t1 - t0 + kTile - 1) / kTile;
     const int b = misc[kB];
 
@@ -306,27 +402,31 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
 
     if (warp == NC) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
+        if (paged || lane == 0) {
             for (int i = issued; i < n_tiles; ++i) {
                 const int s = i % NS;
-                if (!mbar_wait(smem_addr(&bars[NS + s]), ((i / NS) - 1) & 1, p.timeout_ns)) {
-                    misc[kAbort] = 1;
-                    report(p.status, FD_ERR_TIMEOUT);
-                    break;
+                int32_t ya = 0, yb = 0;
+                tile_rows(i, ya, yb);
+                int go = 0;
+                if (lane == 0) {
+                    go = mbar_wait(smem_addr(&bars[NS + s]), ((i / NS) - 1) & 1, p.timeout_ns);
+                    if (!go) {
+                        misc[kAbort] = 1;
+                        report(p.status, FD_ERR_TIMEOUT);
+                    } else if (misc[kAbort]) {
+                        go = 0;
+                    }
                 }
-                if (misc[kAbort])
+                if constexpr (paged)
+                    go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go)
                     break;
-                const uint32_t full = smem_addr(&bars[s]);
-                const uint32_t dst = smem_addr(smem + s * kStageBytes);
-                const int32_t y = t0 + i * kTile;
-                mbar_arrive_expect_tx(full, kStageBytes);
-                tma_load_2d(dst, &tm_k, x_col, y, full, pol);
-                tma_load_2d(dst + kHalfBytes, &tm_k, x_col + 64, y, full, pol);
-                tma_load_2d(dst + 2 * kHalfBytes, &tm_v, x_col, y, full, pol);
-                tma_load_2d(dst + 3 * kHalfBytes, &tm_v, x_col + 64, y, full, pol);
+                if (lane == 0)
+                    issue_tile(i, ya, yb);
                 issued = i + 1;
             }
-            misc[kIssued] = issued;
+            if (lane == 0)
+                misc[kIssued] = issued;
         }
     } else {
         // ---------------------------------------------------------- consumers
@@ -563,14 +663,14 @@ constexpr int kNC = FD_SPLIT_CONSUMER_WARPS;
 constexpr int kNS = FD_SPLIT_STAGES;
 constexpr int kMinCtas = FD_SPLIT_CTAS_PER_SM;
 
-template <int G>
+template <int G, bool PAGED>
 cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitParams &p,
                      int num_work, cudaStream_t stream)
 {
     using L = Layout<G, kNC, kNS>;
     static_assert(kMinCtas * (L::kAlloc + 1024) <= 233472,
                   "the resident CTAs must fit in shared memory");
-    auto kern = split_kv_kernel<G, kNC, kNS, kMinCtas>;
+    auto kern = split_kv_kernel<G, kNC, kNS, kMinCtas, PAGED>;
     // The shared-memory opt-in is per device; remember it for the first 64.
     static bool configured[64] = {};
     int dev = 0;
@@ -607,11 +707,16 @@ int split_ctas_per_sm()
 cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
                          int group, int num_work, cudaStream_t stream)
 {
+    const bool paged = p.kv_last_len != nullptr;
     switch (group) {
-    case 1: return launch_g<1>(tm_k, tm_v, p, num_work, stream);
-    case 2: return launch_g<2>(tm_k, tm_v, p, num_work, stream);
-    case 4: return launch_g<4>(tm_k, tm_v, p, num_work, stream);
-    case 8: return launch_g<8>(tm_k, tm_v, p, num_work, stream);
+    case 1: return paged ? launch_g<1, true>(tm_k, tm_v, p, num_work, stream)
+                         : launch_g<1, false>(tm_k, tm_v, p, num_work, stream);
+    case 2: return paged ? launch_g<2, true>(tm_k, tm_v, p, num_work, stream)
+                         : launch_g<2, false>(tm_k, tm_v, p, num_work, stream);
+    case 4: return paged ? launch_g<4, true>(tm_k, tm_v, p, num_work, stream)
+                         : launch_g<4, false>(tm_k, tm_v, p, num_work, stream);
+    case 8: return paged ? launch_g<8, true>(tm_k, tm_v, p, num_work, stream)
+                         : launch_g<8, false>(tm_k, tm_v, p, num_work, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -117,3 +117,38 @@ def test_plan_with_explicit_sms_needs_no_gpu():
     info = fd.plan(2, 32, 8, 128, [0, 1000, 3000], num_sms=152)
     assert info.num_sms == 152 and info.ctas_per_sm == 2
     assert info.timeout_ns == fd.DEFAULT_TIMEOUT_NS
+
+
+def _prototypes():
+    """name -> list of parameter declarations, parsed from include/fd.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    protos = {}
+    for m in re.finditer(r"\b(fd_[a-z_]+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        protos[m.group(1)] = [] if params == ["void"] else params
+    return protos
+
+
+def _kind(decl: str):
+    if "*" in decl:
+        return "ptr"
+    if "int64_t" in decl or "size_t" in decl:
+        return "i64"
+    if "float" in decl:
+        return "f32"
+    return "i32"
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature has the header's arity and parameter kinds, so a
+    header change that the binding misses fails here rather than on a GPU."""
+    to_kind = {ctypes.c_int: "i32", ctypes.c_int64: "i64", ctypes.c_float: "f32"}
+    protos = _prototypes()
+    assert set(protos) == set(fd.SIGNATURES)
+    for name, params in protos.items():
+        args, _ = fd.SIGNATURES[name]
+        assert len(args) == len(params), f"{name}: {len(args)} ctypes args, header {len(params)}"
+        for i, (a, decl) in enumerate(zip(args, params)):
+            got = to_kind.get(a, "ptr")
+            assert got == _kind(decl), f"{name} arg {i} ({decl}): binding {a}"

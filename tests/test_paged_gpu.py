@@ -1,0 +1,92 @@
+"""Paged KV cache on the GPU (fd_decode_paged) against the fp64 oracle read
+through the page table, and against fd_decode on the same keys laid out
+ragged.
+
+FD++ §6 (vLLM integration): the engine's page table maps each request's keys
+onto fixed-size physical pages, and each split chunk streams the pages its
+keys fall in.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_flashdecoding_gb300 as fd
+from tests.parity_util import assert_within, errors, to_device
+from workloads import make_inputs, make_small, to_paged
+
+pytestmark = pytest.mark.gpu
+
+TIGHT = dict(max_abs=1e-4, rel_l2=1e-5, lse_abs=2e-5)
+
+CASES = [
+    ("ragged_gqa", 4, 32, 8, [1000, 1, 0, 2500]),
+    ("mha", 2, 8, 8, [700, 4096]),
+    ("g8_long", 2, 64, 8, [9000, 2500]),
+    ("g2_tiny", 3, 4, 2, [17, 33, 64]),
+]
+
+
+def _paged_dev(pg, dev):
+    return {k: pg[k].to(dev) for k in ("q", "k_pages", "v_pages", "kv_page_indptr",
+                                       "kv_page_indices", "kv_last_page_len")}
+
+
+def _decode_paged(pg, d, ws=None):
+    return fd.decode_paged(d["q"], d["k_pages"], d["v_pages"], pg["kv_page_indptr"],
+                           pg["kv_last_page_len"], d["kv_page_indptr"], d["kv_last_page_len"],
+                           d["kv_page_indices"], pg["scale"], workspace=ws)
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 48, 64, 256])
+@pytest.mark.parametrize("name,B,Hq,Hkv,lengths", CASES, ids=[c[0] for c in CASES])
+def test_paged_matches_oracle_and_ragged(cuda_device, page_size, name, B, Hq, Hkv, lengths):
+    inp = make_small(B, Hq, Hkv, 128, lengths, seed=len(name) * 31 + page_size)
+    pg = to_paged(inp, page_size, seed=page_size + 1)
+    d = _paged_dev(pg, cuda_device)
+    info = fd.plan_paged(B, Hq, Hkv, 128, page_size, pg["kv_page_indptr"], pg["kv_last_page_len"])
+    ws = torch.zeros(info.workspace_bytes, dtype=torch.uint8, device=cuda_device)
+    o, lse = _decode_paged(pg, d, ws)
+    torch.cuda.synchronize()
+    assert fd.get_device_status(ws) == 0
+    K, V, ip = oracle.gather_paged(pg["k_pages"], pg["v_pages"], pg["kv_page_indptr"],
+                                   pg["kv_page_indices"], pg["kv_last_page_len"])
+    o_ref, lse_ref = oracle.decode(inp["q"], K, V, ip, inp["scale"])
+    err = errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
+    assert_within(err, what=f"{name} P={page_size}")
+    assert_within(err, **TIGHT, what=f"{name} P={page_size} (tight)")
+    # the same keys laid out ragged go through the same splits: identical bits
+    r = to_device(inp, cuda_device)
+    o_r, lse_r = fd.decode(r["q"], r["k"], r["v"], inp["kv_indptr"], r["kv_indptr_dev"], inp["scale"])
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_r) and torch.equal(lse, lse_r)
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_paged_full_size_64k(cuda_device, page_size):
+    """The 64k-context GQA workload (B=1, Hq=32, Hkv=8) in 16- and 64-key pages."""
+    inp = make_inputs(1)
+    pg = to_paged(inp, page_size, seed=11)
+    d = _paged_dev(pg, cuda_device)
+    o, lse = _decode_paged(pg, d)
+    torch.cuda.synchronize()
+    rows = np.arange(0, 32, 3)
+    o_ref, lse_ref = oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"],
+                                   rows=rows)
+    assert_within(errors(o.reshape(32, 128).cpu().numpy()[rows], lse.reshape(32).cpu().numpy()[rows],
+                         o_ref, lse_ref), what=f"64k P={page_size}")
+
+
+def test_page_index_outside_pool_is_flagged(cuda_device):
+    """A page index past the pool sets FD_ERR_DEVICE_BOUNDS; the page is not read."""
+    inp = make_small(1, 8, 8, 128, [200], seed=5)
+    pg = to_paged(inp, 32, seed=2)
+    bad = pg["kv_page_indices"].clone()
+    bad[2] = pg["k_pages"].shape[0] + 7
+    d = _paged_dev(pg, cuda_device)
+    d["kv_page_indices"] = bad.to(cuda_device)
+    info = fd.plan_paged(1, 8, 8, 128, 32, pg["kv_page_indptr"], pg["kv_last_page_len"])
+    ws = torch.zeros(info.workspace_bytes, dtype=torch.uint8, device=cuda_device)
+    o, lse = _decode_paged(pg, d, ws)
+    assert fd.get_device_status(ws) == -6
+    assert torch.isfinite(o).all()

@@ -162,3 +162,46 @@ def make_small(batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
     return dict(q=q, k=k, v=v, kv_indptr=torch.from_numpy(indptr.astype(np.int32)),
                 lengths=list(lengths), scale=fp32_scale(head_dim))
 
+
+
+def to_paged(inp: dict, page_size: int, *, seed: int = 7, spare_pages: int = 3) -> dict:
+    """Lay a ragged input out as a paged KV cache (layout only, no arithmetic).
+
+    Each request's keys fill ceil(L / page_size) pages in order; the pages are
+    scattered over a pool of all used pages plus `spare_pages` unused ones in a
+    seeded random order, so no request's pages are contiguous.  Returns the
+    pools k_pages/v_pages [num_pages, page_size, Hkv, D] (unused rows zero),
+    kv_page_indptr [B+1], kv_page_indices, kv_last_page_len [B] (int32).
+    """
+    k, v = inp["k"], inp["v"]
+    ip = [int(x) for x in inp["kv_indptr"]]
+    B = len(ip) - 1
+    lens = [ip[b + 1] - ip[b] for b in range(B)]
+    pages_per = [(L + page_size - 1) // page_size for L in lens]
+    used = sum(pages_per)
+    num_pages = used + spare_pages
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)[:used].tolist()
+    Hkv, D = k.shape[1], k.shape[2]
+    k_pages = torch.zeros((num_pages, page_size, Hkv, D), dtype=k.dtype)
+    v_pages = torch.zeros((num_pages, page_size, Hkv, D), dtype=v.dtype)
+    page_indptr = np.zeros(B + 1, dtype=np.int64)
+    page_indptr[1:] = np.cumsum(pages_per)
+    indices = np.array(perm, dtype=np.int32)
+    last_len = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        for j in range(pages_per[b]):
+            phys = perm[int(page_indptr[b]) + j]
+            t0 = ip[b] + j * page_size
+            t1 = min(t0 + page_size, ip[b + 1])
+            k_pages[phys, : t1 - t0] = k[t0:t1]
+            v_pages[phys, : t1 - t0] = v[t0:t1]
+        if pages_per[b]:
+            last_len[b] = lens[b] - (pages_per[b] - 1) * page_size
+    out = dict(inp)
+    out.update(k_pages=k_pages, v_pages=v_pages, page_size=page_size,
+               kv_page_indptr=torch.from_numpy(page_indptr.astype(np.int32)),
+               kv_page_indices=torch.from_numpy(indices),
+               kv_last_page_len=torch.from_numpy(last_len))
+    return out
