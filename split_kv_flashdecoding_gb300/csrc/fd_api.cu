@@ -45,42 +45,26 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // K or V [rows, Hkv, 128] bf16 (rows = T keys, or num_pages * page_size for a
-// page pool), 128-byte swizzle, zero fill past the last row.
-//  box_rows == 32: a 3-D map (64 columns, rows, Hkv * 2 column blocks of 64)
-//    whose box (64, 32, 2) brings both 64-column halves of one head's 32 rows
-//    in one copy, laid out in shared memory as [half][row][64].  The block
-//    dimension is last with a 128-byte stride, smaller than the row stride:
-//    TMA takes any 16-byte-multiple strides.
-//  box_rows == 16: a 2-D map of rows x Hkv*128 columns, box 16 rows x 64
-//    columns (one copy per half; the two halves of a 16-row box are not
-//    adjacent in the [half][32 rows][64] stage layout).
+// page pool) as a 3-D tensor (64 columns, rows, Hkv * 2 blocks of 64 columns),
+// 128-byte swizzle, zero fill past the last row.  One box (64, box_rows, 2)
+// brings both 64-column halves of one head's box_rows rows (32, or 16 for
+// pages that are not a multiple of 32 keys) in one copy, laid out in shared
+// memory as [half][row][64].  The block dimension comes last with a 128-byte
+// stride, smaller than the row stride: TMA takes any 16-byte-multiple strides.
 int make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int num_kv_heads,
                 int box_rows = kBoxRows)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
         return FD_ERR_CUDA;
-    const cuuint64_t row_stride = (cuuint64_t)num_kv_heads * kHeadDim * 2;
-    CUresult r;
-    if (box_rows == kBoxRows) {
-        const cuuint64_t dims[3] = {kBoxCols, (cuuint64_t)rows, (cuuint64_t)num_kv_heads * 2};
-        const cuuint64_t strides[2] = {row_stride, kBoxCols * 2};
-        const cuuint32_t box[3] = {kBoxCols, (cuuint32_t)box_rows, 2};
-        const cuuint32_t elem_strides[3] = {1, 1, 1};
-        r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                   strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * kHeadDim, (cuuint64_t)rows};
-        const cuuint64_t strides[1] = {row_stride};
-        const cuuint32_t box[2] = {kBoxCols, (cuuint32_t)box_rows};
-        const cuuint32_t elem_strides[2] = {1, 1};
-        r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                   strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
+    const cuuint64_t dims[3] = {kBoxCols, (cuuint64_t)rows, (cuuint64_t)num_kv_heads * 2};
+    const cuuint64_t strides[2] = {(cuuint64_t)num_kv_heads * kHeadDim * 2, kBoxCols * 2};
+    const cuuint32_t box[3] = {kBoxCols, (cuuint32_t)box_rows, 2};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                              dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
 }
 

@@ -13,9 +13,9 @@
 // Warp roles:
 //   warp NC (producer): one lane issues TMA loads of 32-key tiles of K and V
 //     into an NS-stage ring guarded by full/empty mbarriers.  A tile is one
-//     3-D box per tensor holding both 64-column halves of the head (128-byte
-//     swizzle), or, for a paged cache with 16-key pages, two 2-D boxes of 16
-//     rows per half.
+//     3-D box per tensor holding both 64-column halves of the head's 32 rows
+//     (128-byte swizzle), or, for a paged cache whose pages are not a
+//     multiple of 32 keys, two such boxes of 16 rows.
 //   warps 0..NC-1 (consumers): warp w takes tiles w, w+NC, ...  NS is a
 //     multiple of NC, so every stage always goes to the same warp and a warp
 //     never waits on a barrier more than one phase ahead (parity waits can only
@@ -37,6 +37,7 @@
 // and instruction issue, not by HBM; the contraction itself stays tiny
 // (m = G <= 8 rows).
 #include <cuda/atomic>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,8 +47,24 @@
 namespace fd {
 namespace {
 
-constexpr int kHalfBytes = kTile * 128;        // 32 keys x 64 bf16 (one swizzled box)
+constexpr int kHalfBytes = kTile * 128;        // 32 keys x 64 bf16
 constexpr int kStageBytes = 4 * kHalfBytes;    // K lo, K hi, V lo, V hi
+
+// How K/V rows are found and how a stage is laid out.  A stage holds K then
+// V (kStageBytes / 2 each); key row r (0..31), column half h (64 columns of
+// 128 bytes, 16-byte chunks XOR-swizzled by r % 8) of a tensor sits at
+//   h * HalfStride + (r / 16) * BlockStride + (r % 16) * 128.
+//   kKvRagged, kKvPaged:  [half][32 rows]            HalfStride 4096, BlockStride 2048
+//   kKvPaged16:           [16-row block][half][16]   HalfStride 2048, BlockStride 4096
+// (kKvPaged16 is what one 16-row box of both halves per page lands as.)
+enum KvLayout { kKvRagged = 0, kKvPaged = 1, kKvPaged16 = 2 };
+
+template <int KV>
+struct StageLayout {
+    static constexpr int kHalfStride = KV == kKvPaged16 ? 2048 : kHalfBytes;
+    static constexpr int kBlockStride = KV == kKvPaged16 ? 4096 : 2048;
+    static constexpr int kBoxRows = KV == kKvPaged16 ? 16 : kTile;
+};
 constexpr int kMaxGroup = 8;                   // rows 8-15 of the MMA carry the lo part of P
 
 enum Misc { kB, kPrefix, kSplits, kS, kT0, kT1, kOk, kAbort, kIssued, kLast, kMiscCount };
@@ -212,7 +229,7 @@ __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, in
     }
 }
 
-template <int G, int NC, int NS, int MIN_CTAS, bool PAGED>
+template <int G, int NC, int NS, int MIN_CTAS, int KV>
 __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     split_kv_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -243,8 +260,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     // window of page ids); lane 0 issues the barrier operations and the
     // copies.  The ragged layout needs lane 0 alone.  Key positions t0, t1 are
     // relative to the request's first key.
-    const int32_t x_col = kvh * kHeadDim;
-    constexpr bool paged = PAGED;
+    constexpr bool paged = KV != kKvRagged;
+    using SL = StageLayout<KV>;
     uint64_t pol = 0;
     int issued = 0;
     int32_t t0 = 0, t1 = 0, req_base = 0, req_len = 0, req_pages = 0;
@@ -279,7 +296,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         // Rows past the request's last key read whatever its last page holds
         // there; the consumers mask them.
         const int32_t y = page_id(min(cur_pg, req_pages - 1)) * p.page_size + cur_off;
-        cur_off += p.box_rows;
+        cur_off += SL::kBoxRows;
         if (cur_off >= p.page_size) {
             cur_off -= p.page_size;
             ++cur_pg;
@@ -295,31 +312,22 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
             ya = req_base + t0 + i * kTile;
         } else {
             ya = next_box_row();
-            if (p.box_rows < kTile)
+            if constexpr (SL::kBoxRows < kTile)
                 yb = next_box_row();
         }
     };
-    // Lane 0: put tile i into stage i % NS.  Whole-tile boxes use the 3-D maps
-    // (both 64-column halves in one box); 16-row boxes use 2-D maps, one per
-    // half, the second box 16 rows further into the stage.
+    // Lane 0: put tile i into stage i % NS: one 3-D box of both 64-column
+    // halves per tensor and per box of rows (one box, or two of 16 rows).
     auto issue_tile = [&](int i, int32_t ya, int32_t yb) {
         const int s = i % NS;
         const uint32_t full = smem_addr(&bars[s]);
         const uint32_t dst = smem_addr(smem + s * kStageBytes);
         mbar_arrive_expect_tx(full, kStageBytes);
-        if (!paged || p.box_rows == kTile) {
-            tma_load_3d(dst, &tm_k, 0, ya, 2 * kvh, full, pol);
-            tma_load_3d(dst + 2 * kHalfBytes, &tm_v, 0, ya, 2 * kvh, full, pol);
-        } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int32_t y = h ? yb : ya;
-                const uint32_t off = h * (kTile / 2) * 128;
-                tma_load_2d(dst + off, &tm_k, x_col, y, full, pol);
-                tma_load_2d(dst + kHalfBytes + off, &tm_k, x_col + 64, y, full, pol);
-                tma_load_2d(dst + 2 * kHalfBytes + off, &tm_v, x_col, y, full, pol);
-                tma_load_2d(dst + 3 * kHalfBytes + off, &tm_v, x_col + 64, y, full, pol);
-            }
+        tma_load_3d(dst, &tm_k, 0, ya, 2 * kvh, full, pol);
+        tma_load_3d(dst + 2 * kHalfBytes, &tm_v, 0, ya, 2 * kvh, full, pol);
+        if constexpr (SL::kBoxRows < kTile) {
+            tma_load_3d(dst + SL::kBlockStride, &tm_k, 0, yb, 2 * kvh, full, pol);
+            tma_load_3d(dst + 2 * kHalfBytes + SL::kBlockStride, &tm_v, 0, yb, 2 * kvh, full, pol);
         }
     };
 
@@ -466,13 +474,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                 sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
 #pragma unroll
             for (int kp = 0; kp < 4; ++kp) {           // 32 columns per ldmatrix.x4
-                const uint32_t half = st + (kp >> 1) * kHalfBytes;
+                const uint32_t half = st + (kp >> 1) * SL::kHalfStride;
                 const int chunk = 4 * (kp & 1) + lm;   // matrix lm = columns 8*lm .. +7
 #pragma unroll
                 for (int jn = 0; jn < 4; ++jn) {
-                    const int row = 8 * jn + lr;
+                    // key row 8 jn + lr: block jn / 2, row 8 (jn % 2) + lr in it
+                    const uint32_t row_off = (jn >> 1) * SL::kBlockStride + (8 * (jn & 1) + lr) * 128;
                     uint32_t kb[4];
-                    ldsm_x4(half + row * 128 + ((chunk ^ lr) << 4), kb);
+                    ldsm_x4(half + row_off + ((chunk ^ lr) << 4), kb);
                     mma_bf16(sc[jn], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, kb[0], kb[1]);
                     mma_bf16(sc[jn], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, kb[2], kb[3]);
                 }
@@ -529,13 +538,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
             // ---- O += P V : 2 k-steps of 16 keys, 16 n-tiles of 8 columns
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
-                const int row = 16 * ks + 8 * (lm & 1) + lr;   // matrix lm: keys 8*(lm&1) ..
+                // matrix lm: keys 16 ks + 8 (lm & 1) + lr = block ks, row 8 (lm & 1) + lr
+                const uint32_t row_off = ks * SL::kBlockStride + (8 * (lm & 1) + lr) * 128;
 #pragma unroll
                 for (int np = 0; np < 8; ++np) {                // 16 columns per ldmatrix.x4
-                    const uint32_t half = st + 2 * kHalfBytes + (np >> 2) * kHalfBytes;
+                    const uint32_t half = st + 2 * kHalfBytes + (np >> 2) * SL::kHalfStride;
                     const int chunk = 2 * (np & 3) + (lm >> 1);  // columns 8*(lm>>1) ..
                     uint32_t vb[4];
-                    ldsm_x4_trans(half + row * 128 + ((chunk ^ lr) << 4), vb);
+                    ldsm_x4_trans(half + row_off + ((chunk ^ lr) << 4), vb);
                     mma_bf16(o_acc[2 * np], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], vb[0], vb[1]);
                     mma_bf16(o_acc[2 * np + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], vb[2],
                              vb[3]);
@@ -663,14 +673,14 @@ constexpr int kNC = FD_SPLIT_CONSUMER_WARPS;
 constexpr int kNS = FD_SPLIT_STAGES;
 constexpr int kMinCtas = FD_SPLIT_CTAS_PER_SM;
 
-template <int G, bool PAGED>
+template <int G, int KV>
 cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitParams &p,
                      int num_work, cudaStream_t stream)
 {
     using L = Layout<G, kNC, kNS>;
     static_assert(kMinCtas * (L::kAlloc + 1024) <= 233472,
                   "the resident CTAs must fit in shared memory");
-    auto kern = split_kv_kernel<G, kNC, kNS, kMinCtas, PAGED>;
+    auto kern = split_kv_kernel<G, kNC, kNS, kMinCtas, KV>;
     // The shared-memory opt-in is per device; remember it for the first 64.
     static bool configured[64] = {};
     int dev = 0;
@@ -707,16 +717,22 @@ int split_ctas_per_sm()
 cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
                          int group, int num_work, cudaStream_t stream)
 {
-    const bool paged = p.kv_last_len != nullptr;
+    const int kv = p.kv_last_len == nullptr ? kKvRagged
+                   : p.box_rows == kTile    ? kKvPaged
+                                            : kKvPaged16;
+    auto by_layout = [&](auto g) -> cudaError_t {
+        constexpr int G = decltype(g)::value;
+        switch (kv) {
+        case kKvRagged: return launch_g<G, kKvRagged>(tm_k, tm_v, p, num_work, stream);
+        case kKvPaged: return launch_g<G, kKvPaged>(tm_k, tm_v, p, num_work, stream);
+        default: return launch_g<G, kKvPaged16>(tm_k, tm_v, p, num_work, stream);
+        }
+    };
     switch (group) {
-    case 1: return paged ? launch_g<1, true>(tm_k, tm_v, p, num_work, stream)
-                         : launch_g<1, false>(tm_k, tm_v, p, num_work, stream);
-    case 2: return paged ? launch_g<2, true>(tm_k, tm_v, p, num_work, stream)
-                         : launch_g<2, false>(tm_k, tm_v, p, num_work, stream);
-    case 4: return paged ? launch_g<4, true>(tm_k, tm_v, p, num_work, stream)
-                         : launch_g<4, false>(tm_k, tm_v, p, num_work, stream);
-    case 8: return paged ? launch_g<8, true>(tm_k, tm_v, p, num_work, stream)
-                         : launch_g<8, false>(tm_k, tm_v, p, num_work, stream);
+    case 1: return by_layout(std::integral_constant<int, 1>{});
+    case 2: return by_layout(std::integral_constant<int, 2>{});
+    case 4: return by_layout(std::integral_constant<int, 4>{});
+    case 8: return by_layout(std::integral_constant<int, 8>{});
     default: return cudaErrorInvalidValue;
     }
 }
