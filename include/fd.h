@@ -42,9 +42,12 @@
  * to a status word in the workspace and read by fd_get_device_status().
  *
  * Workspace: a caller-owned device buffer, zero-filled before its first use.
- * Its first FD_WORKSPACE_HEADER_BYTES hold the device status word; fd_decode
- * also keeps in it one merge ticket per (request, KV head) and the split
- * partials (size: fd_plan_info.workspace_bytes).  The tickets return to zero
+ * Its first FD_WORKSPACE_HEADER_BYTES hold the device status word and the
+ * work counter of the split kernel (used when a plan has more split items than
+ * one wave of resident CTAs: the kernel then runs persistent CTAs that claim
+ * items from the counter); fd_decode also keeps in it one merge ticket per
+ * (request, KV head) and the split partials (size:
+ * fd_plan_info.workspace_bytes).  The counter and the tickets return to zero
  * at the end of every successful call; after a call that reported an error
  * status, zero the workspace again before reusing it.  Calls that share one
  * workspace must be ordered on one stream.
@@ -166,7 +169,7 @@ int fd_plan_work_items(const fd_plan_info *info, const int32_t *kv_indptr_host,
  *
  * info: from fd_plan for this kv_indptr.  kv_indptr_dev: device copy of the
  * same indptr.  scale: softmax scale (applied to q.k).  workspace: device,
- * >= FD_WORKSPACE_HEADER_BYTES (status word).
+ * >= FD_WORKSPACE_HEADER_BYTES (status word, work counter).
  */
 int fd_decode_split(const fd_plan_info *info, const void *q, const void *k,
                     const void *v, const int32_t *kv_indptr_dev, float scale,
@@ -262,7 +265,7 @@ int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
  * need in fd_plan_info.workspace_bytes); use fd_decode with a workspace then.
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  Each call
- * clears the status word and the merge tickets on its stream before it runs.
+ * clears the workspace header and the merge tickets on its stream before it runs.
  * All calls share the one array, which keeps the last call's contents: calls
  * that can overlap on the GPU (other streams, other host threads, without
  * ordering between them) race and give wrong results.  The status word is

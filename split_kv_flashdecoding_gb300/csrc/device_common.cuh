@@ -131,6 +131,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch
 
 // Allow the next grid in the stream (launched with programmatic stream
@@ -253,5 +263,66 @@ __device__ __forceinline__ bool derive_split(const KeyIndex &ki, int batch, int3
     }
     return false;
 }
+
+// Warp-collective cursor over all requests' splits for a sequence of split
+// indices that never decreases (the items of one persistent CTA).  Lane l holds
+// request b0 + l of the current window of 32 requests and the inclusive prefix
+// of the split counts; moving on to the next window costs one load per lane,
+// so a batch of at most 32 requests is read once per CTA.
+struct SplitCursor {
+    int32_t b0 = 0;      // first request of the window
+    int32_t carry = 0;   // splits of the requests before b0
+    int32_t base = 0, len = 0, pages = 0, n = 0, incl = 0;
+    bool loaded = false;
+
+    __device__ __forceinline__ void load(const KeyIndex &ki, int batch, int32_t chunk)
+    {
+        const int lane = threadIdx.x & 31;
+        const int b = b0 + lane;
+        base = len = pages = n = 0;
+        if (b < batch) {
+            ki.at(b, base, len, pages);
+            n = splits_for(len, chunk);
+        }
+        incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += t;
+        }
+        incl += carry;
+        loaded = true;
+    }
+
+    // Locate global split j (not below any j asked before); false if j is
+    // past the last split.
+    __device__ __forceinline__ bool find(const KeyIndex &ki, int batch, int32_t chunk, int32_t j,
+                                         SplitCoord &out)
+    {
+        const int lane = threadIdx.x & 31;
+        while (b0 < batch) {
+            if (!loaded)
+                load(ki, batch, chunk);
+            const int32_t excl = incl - n;
+            const unsigned mask = __ballot_sync(0xffffffffu, b0 + lane < batch && j >= excl && j < incl);
+            if (mask) {
+                const int src = __ffs(mask) - 1;
+                out.b = b0 + src;
+                out.prefix = __shfl_sync(0xffffffffu, excl, src);
+                out.splits = __shfl_sync(0xffffffffu, n, src);
+                out.base = __shfl_sync(0xffffffffu, base, src);
+                out.len = __shfl_sync(0xffffffffu, len, src);
+                out.pages = __shfl_sync(0xffffffffu, pages, src);
+                out.s = j - out.prefix;
+                return true;
+            }
+            carry = __shfl_sync(0xffffffffu, incl, 31);
+            b0 += 32;
+            loaded = false;
+        }
+        return false;
+    }
+};
 
 }  // namespace fd

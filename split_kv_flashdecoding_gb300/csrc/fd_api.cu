@@ -17,6 +17,9 @@ namespace {
 
 constexpr int kHeadDim = 128;
 constexpr int kBoxCols = 64;     // one 128-byte swizzle span of bf16
+// Workspace header: the status word at byte 0, the split kernel's item-claim
+// counter at byte 64 (a sector of its own).
+constexpr int kClaimOffset = 64;
 constexpr int kBoxRows = FD_TILE_TOKENS;
 
 bool aligned(const void *p, uintptr_t a)
@@ -180,6 +183,7 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.partial_o = partial_o;
     p.partial_lse = partial_lse;
     p.status = static_cast<int *>(workspace);
+    p.claim = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + kClaimOffset);
     p.batch = info->batch;
     p.num_qo_heads = info->num_qo_heads;
     p.num_kv_heads = info->num_kv_heads;
@@ -208,8 +212,11 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.num_page_entries = paged ? paged->num_page_entries : 0;
     if (paged && p.indptr_in_params)
         memcpy(p.last_len_param, paged->last_len_host, (size_t)info->batch * sizeof(int32_t));
-    const cudaError_t e =
-        fd::launch_split(tm_k, tm_v, p, info->group_size, info->num_work, stream);
+    // Persistent grid: at most one wave of resident CTAs on the plan's SMs.
+    p.num_work = info->num_work;
+    const int64_t slots = (int64_t)info->num_sms * fd::split_ctas_per_sm();
+    const int num_ctas = slots > 0 && slots < info->num_work ? (int)slots : info->num_work;
+    const cudaError_t e = fd::launch_split(tm_k, tm_v, p, info->group_size, num_ctas, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 

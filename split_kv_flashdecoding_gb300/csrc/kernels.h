@@ -22,6 +22,7 @@ struct SplitParams {
     int32_t num_kv_heads;
     int32_t chunk;
     int32_t num_partial_rows;
+    int32_t num_work;           // items: total splits x KV heads
     int32_t total_tokens;
     float q_scale;              // softmax scale * log2(e): logits are kept in base 2
     int64_t timeout_ns;
@@ -32,6 +33,10 @@ struct SplitParams {
     float *o;                   // [B, Hq, D]
     float *lse;                 // [B, Hq]
     int *counters;
+    // Persistent grid: items past the first wave are claimed from this
+    // zero-initialised counter (in the workspace header); the CTA that makes
+    // the last claim resets it.
+    int *claim;
     int32_t indptr_in_params;   // 1: indptr_param (and last_len_param) hold the device arrays
     int32_t indptr_param[kParamIndptr];
     // Paged KV (kv_last_len non-null): K/V are page pools [num_pages, page_size,
@@ -61,11 +66,12 @@ struct MergeParams {
     int32_t page_size;
 };
 
-// Stage 1: one CTA per (split, KV head); grid = num_work.  Launched as a
-// programmatic dependent of the preceding grid (it waits for that grid before
-// touching global memory).
+// Stage 1: p.num_work items (split, KV head) on a persistent grid of num_ctas
+// CTAs (1 <= num_ctas <= p.num_work), CTA c taking items c, c + num_ctas, ...
+// Launched as a programmatic dependent of the preceding grid (it waits for
+// that grid before touching global memory).
 cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
-                         int group, int num_work, cudaStream_t stream);
+                         int group, int num_ctas, cudaStream_t stream);
 
 // Resident split-kernel CTAs per SM the launch shape is built for.
 int split_ctas_per_sm();

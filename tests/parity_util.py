@@ -48,7 +48,8 @@ def to_device(inp: dict, device) -> dict:
     return out
 
 
-def two_stage(dev_inp: dict, *, chunk=0, ctas_per_sm=0, guard=0, stream=None, timeout_ns=None):
+def two_stage(dev_inp: dict, *, chunk=0, ctas_per_sm=0, num_sms=0, guard=0, stream=None,
+              timeout_ns=None):
     """Plan + fd_decode_split + fd_merge through the C ABI.
 
     With guard > 0 every output buffer sits inside a larger one whose extra
@@ -58,7 +59,7 @@ def two_stage(dev_inp: dict, *, chunk=0, ctas_per_sm=0, guard=0, stream=None, ti
     B, Hq, D = q.shape
     Hkv = k.shape[1]
     info = fd.plan(B, Hq, Hkv, D, dev_inp["kv_indptr"], chunk=chunk, ctas_per_sm=ctas_per_sm,
-                   timeout_ns=timeout_ns)
+                   num_sms=num_sms, timeout_ns=timeout_ns)
     dev = q.device
     rows = info.num_partial_rows
     g = guard * 128   # whole rows of 128 floats keep interior pointers 16-byte aligned

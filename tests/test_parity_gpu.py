@@ -56,6 +56,28 @@ def test_two_stage_small(cuda_device, name, B, Hq, Hkv, lengths, chunk):
     assert_within(err, **TIGHT, what=name + " (tight)")
 
 
+@pytest.mark.parametrize("num_sms", [1, 3])
+@pytest.mark.parametrize("name,B,Hq,Hkv,lengths", SMALL_CASES[4:7], ids=[c[0] for c in SMALL_CASES[4:7]])
+def test_persistent_ctas_run_many_items(cuda_device, num_sms, name, B, Hq, Hkv, lengths):
+    """A plan for 1 or 3 SMs launches 2 or 6 persistent CTAs, each running
+    many items back to back (the stage ring and the item-descriptor ring wrap
+    many times): the partials are bit-identical to the default grid's and the
+    result matches the oracle."""
+    inp = make_small(B, Hq, Hkv, 128, lengths, seed=zlib.crc32(name.encode()) % 1000 + num_sms)
+    dev = to_device(inp, cuda_device)
+    few = two_stage(dev, chunk=32, num_sms=num_sms, guard=2)
+    full = two_stage(dev, chunk=32)
+    torch.cuda.synchronize()
+    assert fd.get_device_status(few["ws"]) == 0 and fd.get_device_status(full["ws"]) == 0
+    check_guards(few)
+    assert few["info"].num_work >= 8 * num_sms * few["info"].ctas_per_sm
+    assert torch.equal(few["partial_o"], full["partial_o"])
+    assert torch.equal(few["partial_lse"], full["partial_lse"])
+    o_ref, lse_ref = _oracle(inp)
+    err = errors(few["o"].cpu().numpy(), few["lse"].cpu().numpy(), o_ref, lse_ref)
+    assert_within(err, **TIGHT, what=name)
+
+
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("chunk", [32, 128, 0])
 def test_split_partials_match_stage1_oracle(cuda_device, G, chunk):
