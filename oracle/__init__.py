@@ -14,6 +14,11 @@ two-stage global reduction".
   gather_paged(...)       a paged KV cache read through its page table into the
                           ragged layout decode() takes (§6: the engine's page
                           table maps each request's keys onto physical pages)
+  e4m3_to_float(codes)    FP8 E4M3 byte codes -> fp64 values (the OCP format
+                          definition; §4: K/V held in FP8 in HBM)
+  dequant_fp8(codes, s)   K or V codes [T, Hkv, D] times a per-KV-head scale
+  decode_fp8(...)         decode() on exactly dequantised FP8 K/V (§4: the
+                          quantised cache is dequantised, then attended over)
 
 The arithmetic is in fd_oracle.c (fp64 throughout); this module only
 marshals arrays.  build() compiles it with gcc.
@@ -214,3 +219,51 @@ def gather_paged(k_pages, v_pages, kv_page_indptr, kv_page_indices, kv_last_page
         return torch.cat(ks), torch.cat(vs), indptr
     shape = (0, k_pages.shape[2], k_pages.shape[3])
     return torch.zeros(shape, dtype=k_pages.dtype), torch.zeros(shape, dtype=v_pages.dtype), indptr
+
+
+def e4m3_to_float(codes) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) -> fp64, from the format definition.
+
+    The OCP 8-bit floating-point format E4M3: 1 sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits, no infinities.  Exponent field 0 is subnormal,
+    (m / 8) * 2^-6; otherwise (1 + m / 8) * 2^(e - 7).  S.1111.111 is NaN, so
+    the largest finite magnitude is 1.75 * 2^8 = 448.
+    """
+    c = np.asarray(codes).astype(np.uint8)
+    sign = (c >> 7) & 1
+    e = ((c >> 3) & 0xF).astype(np.int64)
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+def dequant_fp8(codes, scale) -> np.ndarray:
+    """K or V as E4M3 codes [T, Hkv, D] with one fp32 scale per KV head [Hkv]
+    -> fp64 values code * scale[h] (exact: 4 significant bits times 24)."""
+    try:
+        import torch
+        if isinstance(codes, torch.Tensor):
+            codes = codes.detach().cpu().contiguous().view(torch.uint8).numpy()
+        if isinstance(scale, torch.Tensor):
+            scale = scale.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    vals = e4m3_to_float(codes)
+    s = np.asarray(scale, dtype=np.float32).astype(np.float64).reshape(1, -1, 1)
+    return vals * s
+
+
+def _bf16_to_f64(q) -> np.ndarray:
+    code, a = _as_array(q)
+    if code == 0:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, kv_indptr, scale, rows=None,
+               threads: int | None = None):
+    """decode() on FP8 K/V: both are dequantised exactly (dequant_fp8) and q
+    is widened to fp64, then the same unsplit definition runs in fp64."""
+    return decode(_bf16_to_f64(q), dequant_fp8(k_codes, k_scale), dequant_fp8(v_codes, v_scale),
+                  kv_indptr, scale, rows=rows, threads=threads)

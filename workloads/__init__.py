@@ -205,3 +205,22 @@ def to_paged(inp: dict, page_size: int, *, seed: int = 7, spare_pages: int = 3) 
                kv_page_indices=torch.from_numpy(indices),
                kv_last_page_len=torch.from_numpy(last_len))
     return out
+
+
+def to_fp8(inp: dict) -> dict:
+    """Quantise an input's K and V to FP8 E4M3 (storage layout only).
+
+    Per tensor and KV head h: scale[h] = max |x[:, h, :]| / 448 in fp32 (1 for
+    an all-zero head); codes = E4M3(x / scale[h]) rounded to nearest even,
+    clamped to +-448 so nothing rounds to NaN.  Returns a copy of `inp` with
+    k_fp8, v_fp8 (uint8 [T, Hkv, D]) and k_scale, v_scale (fp32 [Hkv]).
+    """
+    out = dict(inp)
+    for name in ("k", "v"):
+        x = inp[name].float()
+        amax = x.abs().amax(dim=(0, 2)) if x.shape[0] else torch.zeros(x.shape[1])
+        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+        q = (x / scale[None, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+        out[name + "_fp8"] = q.view(torch.uint8).contiguous()
+        out[name + "_scale"] = scale.contiguous()
+    return out
