@@ -49,7 +49,8 @@ L2_FLUSH_BYTES = 1 << 30
 L2_BYTES = 129 * 1000 * 1000       # GB300 L2
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-SPLIT_SOURCES = ["split_kernel.cu", "device_common.cuh", "plan_rule.h", "fd_api.cu"]
+SPLIT_SOURCES = ["split_kernel.cuh", "split_kernel.cu", "split_kernel_fp8.cu", "device_common.cuh",
+                 "plan_rule.h", "fd_api.cu"]
 
 
 # ----------------------------------------------------------------- helpers

@@ -247,6 +247,38 @@ int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                     void *stream);
 
 /*
+ * FP8 (E4M3) KV cache -- FD++ §4 ("quantisation-friendly kernel fusion"): the
+ * quantised K and V are read from HBM as they are and dequantised on chip, in
+ * registers, straight into the tensor-core operands, so the stream moves half
+ * the bytes of bf16.
+ *
+ * Layout: K and V hold one OCP FP8 E4M3 byte per value (1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; no infinities) in the same shapes as the
+ * bf16 entry points ([T, Hkv, D] ragged, [num_pages, page_size, Hkv, D]
+ * paged).  k_scale and v_scale (device, fp32 [Hkv]) give each KV head's
+ * scale: the value of a K byte is E4M3(byte) * k_scale[head], and likewise
+ * for V.  q stays bf16 and O, LSE fp32.  The arithmetic matches the bf16 path
+ * (every E4M3 value is exact in f16, the products accumulate in fp32); the
+ * result is attention over the dequantised K and V.  Byte 0x7F / 0xFF (NaN)
+ * propagates as NaN.  Workspace and plan as for fd_decode / fd_decode_paged.
+ */
+int fd_decode_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                  const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+                  const void *q, const void *k_fp8, const void *v_fp8,
+                  const float *k_scale, const float *v_scale, float scale,
+                  float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                  void *stream);
+
+int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                        int page_size, int num_pages, const int32_t *kv_page_indptr_host,
+                        const int32_t *kv_last_page_len_host, const int32_t *kv_page_indptr_dev,
+                        const int32_t *kv_last_page_len_dev, const int32_t *kv_page_indices_dev,
+                        const void *q, const void *k_pages_fp8, const void *v_pages_fp8,
+                        const float *k_scale, const float *v_scale, float scale,
+                        float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                        void *stream);
+
+/*
  * fd_decode_static_workspace -- fd_decode for callers that cannot allocate.
  *
  * The article has no counterpart: this is a library convenience.  Some

@@ -89,6 +89,9 @@ SIGNATURES = {
     "fd_plan_paged": ([_I, _I, _I, _I, _I, _P, _P, _I, _I, _I, _PI], _I),
     "fd_decode_paged": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P,
                          _P, _I64, _P], _I),
+    "fd_decode_fp8": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
+    "fd_decode_paged_fp8": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F,
+                             _P, _P, _P, _I64, _P], _I),
 }
 
 
@@ -289,6 +292,66 @@ def decode_paged(q, k_pages, v_pages, kv_page_indptr_host, kv_last_page_len_host
     return o, lse
 
 
+def _fp8_bytes(x):
+    """An FP8 K/V tensor as torch gives it (float8_e4m3fn) or as raw uint8."""
+    import torch
+    if x.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise FdError(-1, "FP8 K/V must be uint8 or float8_e4m3fn")
+    return x
+
+
+def decode_fp8(q, k_fp8, v_fp8, k_scale, v_scale, kv_indptr_host, kv_indptr_dev, scale: float, *,
+               o=None, lse=None, workspace=None, stream=None):
+    """fd_decode_fp8: q [B,Hq,D] bf16, k/v [T,Hkv,D] E4M3 bytes (uint8 or
+    float8_e4m3fn), k_scale / v_scale fp32 [Hkv] CUDA tensors -> (O, LSE) fp32."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv = k_fp8.shape[1]
+    ip = _host_indptr(kv_indptr_host)
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = plan(B, Hq, Hkv, D, ip).workspace_bytes
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    _check(lib().fd_decode_fp8(B, Hq, Hkv, D, ip.ctypes.data_as(ctypes.c_void_p), _ptr(kv_indptr_dev),
+                               _ptr(q), _ptr(_fp8_bytes(k_fp8)), _ptr(_fp8_bytes(v_fp8)),
+                               _ptr(k_scale), _ptr(v_scale), float(scale), _ptr(o), _ptr(lse),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream)), "fd_decode_fp8")
+    return o, lse
+
+
+def decode_paged_fp8(q, k_pages_fp8, v_pages_fp8, k_scale, v_scale, kv_page_indptr_host,
+                     kv_last_page_len_host, kv_page_indptr_dev, kv_last_page_len_dev,
+                     kv_page_indices_dev, scale: float, *, o=None, lse=None, workspace=None,
+                     stream=None):
+    """fd_decode_paged_fp8: fd_decode_paged over E4M3 page pools with
+    per-KV-head fp32 scales."""
+    import torch
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv = k_pages_fp8.shape[0], k_pages_fp8.shape[1], k_pages_fp8.shape[2]
+    ip = _host_indptr(kv_page_indptr_host)
+    ll = _host_indptr(kv_last_page_len_host)
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = plan_paged(B, Hq, Hkv, D, page_size, ip, ll).workspace_bytes
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    _check(lib().fd_decode_paged_fp8(B, Hq, Hkv, D, page_size, num_pages,
+                                     ip.ctypes.data_as(ctypes.c_void_p),
+                                     ll.ctypes.data_as(ctypes.c_void_p), _ptr(kv_page_indptr_dev),
+                                     _ptr(kv_last_page_len_dev), _ptr(kv_page_indices_dev), _ptr(q),
+                                     _ptr(_fp8_bytes(k_pages_fp8)), _ptr(_fp8_bytes(v_pages_fp8)),
+                                     _ptr(k_scale), _ptr(v_scale), float(scale), _ptr(o), _ptr(lse),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)), "fd_decode_paged_fp8")
+    return o, lse
+
+
 def get_device_status(workspace, stream=None) -> int:
     """fd_get_device_status: synchronise, read and clear the kernels' status word."""
     return lib().fd_get_device_status(_ptr(workspace), _stream(stream))
@@ -296,7 +359,8 @@ def get_device_status(workspace, stream=None) -> int:
 
 __all__ = [
     "PlanInfo", "FdError", "lib", "build", "plan", "plan_work_items", "decode_split", "merge",
-    "decode", "decode_static_workspace", "plan_paged", "decode_paged", "get_device_status",
+    "decode", "decode_static_workspace", "plan_paged", "decode_paged", "decode_fp8",
+    "decode_paged_fp8", "get_device_status",
     "workspace_bytes", "num_sms",
     "status_string",
     "TILE_TOKENS", "WORKSPACE_HEADER_BYTES", "DEFAULT_TIMEOUT_NS",

@@ -71,6 +71,25 @@ int make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int num_kv_hea
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
 }
 
+// FP8 K or V [rows, Hkv, 128] (one byte per value) as a 2-D tensor of rows x
+// Hkv*128 bytes; one box = box_rows rows x the head's 128 bytes, 128-byte
+// swizzle, zero fill past the last row.
+int make_kv_map_fp8(CUtensorMap *map, const void *base, int64_t rows, int num_kv_heads, int box_rows)
+{
+    auto encode = tensor_map_encoder();
+    if (!encode)
+        return FD_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * kHeadDim};
+    const cuuint32_t box[2] = {kHeadDim, (cuuint32_t)box_rows};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                              strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
+}
+
 int check_info(const fd_plan_info *info)
 {
     if (!info)
@@ -140,6 +159,12 @@ extern "C" int fd_num_sms(int device, int *num_sms)
 
 namespace {
 
+// FP8 (E4M3) K/V: the per-KV-head scales (device, [Hkv] each).
+struct Fp8KV {
+    const float *k_scale;
+    const float *v_scale;
+};
+
 // The page-pool description of a paged KV cache (see fd_decode_paged).
 struct PagedKV {
     int32_t page_size;
@@ -159,7 +184,7 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
                   const int32_t *kv_indptr_dev, float scale, float *partial_o, float *partial_lse,
                   void *workspace, float *o, float *lse, int *counters,
                   const int32_t *kv_indptr_host, cudaStream_t stream,
-                  const PagedKV *paged = nullptr)
+                  const PagedKV *paged = nullptr, const Fp8KV *fp8 = nullptr)
 {
     if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
         return FD_ERR_INVALID_ARG;
@@ -168,14 +193,22 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
         return FD_ERR_INVALID_ARG;
     if (!(scale == scale))
         return FD_ERR_INVALID_ARG;
+    if (fp8 && (!fp8->k_scale || !fp8->v_scale || !aligned(fp8->k_scale, 4) ||
+                !aligned(fp8->v_scale, 4)))
+        return FD_ERR_INVALID_ARG;
 
     CUtensorMap tm_k, tm_v;
     int rc;
     const int64_t rows = paged ? (int64_t)paged->num_pages * paged->page_size : info->total_tokens;
     const int box_rows = paged && paged->page_size % kBoxRows != 0 ? 16 : kBoxRows;
-    if ((rc = make_kv_map(&tm_k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
-        (rc = make_kv_map(&tm_v, v, rows, info->num_kv_heads, box_rows)) != FD_OK)
+    if (fp8) {
+        if ((rc = make_kv_map_fp8(&tm_k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+            (rc = make_kv_map_fp8(&tm_v, v, rows, info->num_kv_heads, box_rows)) != FD_OK)
+            return rc;
+    } else if ((rc = make_kv_map(&tm_k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+               (rc = make_kv_map(&tm_v, v, rows, info->num_kv_heads, box_rows)) != FD_OK) {
         return rc;
+    }
 
     fd::SplitParams p;
     p.q = static_cast<const uint16_t *>(q);
@@ -212,6 +245,9 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.num_page_entries = paged ? paged->num_page_entries : 0;
     if (paged && p.indptr_in_params)
         memcpy(p.last_len_param, paged->last_len_host, (size_t)info->batch * sizeof(int32_t));
+    p.kv_fp8 = fp8 != nullptr;
+    p.k_scale = fp8 ? fp8->k_scale : nullptr;
+    p.v_scale = fp8 ? fp8->v_scale : nullptr;
     // Persistent grid: at most one wave of resident CTAs on the plan's SMs.
     p.num_work = info->num_work;
     const int64_t slots = (int64_t)info->num_sms * fd::split_ctas_per_sm();
@@ -272,10 +308,13 @@ extern "C" int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
-extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-                         const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
-                         const void *q, const void *k, const void *v, float scale, float *o,
-                         float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+namespace {
+
+// fd_decode and fd_decode_fp8 (fp8 non-null).
+int decode_ragged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                  const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev, const void *q,
+                  const void *k, const void *v, float scale, float *o, float *lse, void *workspace,
+                  int64_t workspace_bytes, void *stream, const Fp8KV *fp8)
 {
     fd_plan_info info;
     int rc = fd_plan(batch, num_qo_heads, num_kv_heads, head_dim, kv_indptr_host, 0, 0, 0, &info);
@@ -297,7 +336,7 @@ extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head
     cudaStream_t s = as_stream(stream);
     if (info.num_work > 0) {
         rc = launch_stage1(&info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
-                           o, lse, counters, kv_indptr_host, s);
+                           o, lse, counters, kv_indptr_host, s, nullptr, fp8);
         if (rc != FD_OK)
             return rc;
     }
@@ -324,8 +363,6 @@ extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head
     p.page_size = 0;
     return fd::launch_merge(p, s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
-
-namespace {
 
 // Host checks of a paged layout; fills the logical key-row prefix (keys of
 // request b = (pages_b - 1) * page_size + last_len_b) for the planner.
@@ -370,14 +407,15 @@ extern "C" int fd_plan_paged(int batch, int num_qo_heads, int num_kv_heads, int 
                    ctas_per_sm, chunk, info);
 }
 
-extern "C" int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-                               int page_size, int num_pages, const int32_t *kv_page_indptr_host,
-                               const int32_t *kv_last_page_len_host,
-                               const int32_t *kv_page_indptr_dev,
-                               const int32_t *kv_last_page_len_dev,
-                               const int32_t *kv_page_indices_dev, const void *q,
-                               const void *k_pages, const void *v_pages, float scale, float *o,
-                               float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+namespace {
+
+// fd_decode_paged and fd_decode_paged_fp8 (fp8 non-null).
+int decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                 int num_pages, const int32_t *kv_page_indptr_host,
+                 const int32_t *kv_last_page_len_host, const int32_t *kv_page_indptr_dev,
+                 const int32_t *kv_last_page_len_dev, const int32_t *kv_page_indices_dev,
+                 const void *q, const void *k_pages, const void *v_pages, float scale, float *o,
+                 float *lse, void *workspace, int64_t workspace_bytes, void *stream, const Fp8KV *fp8)
 {
     fd_plan_info info;
     int rc = fd_plan_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size,
@@ -405,7 +443,7 @@ extern "C" int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, in
         const PagedKV pk{page_size, num_pages, kv_last_page_len_dev, kv_last_page_len_host,
                          kv_page_indices_dev, kv_page_indptr_host[batch]};
         rc = launch_stage1(&info, q, k_pages, v_pages, kv_page_indptr_dev, scale, partial_o,
-                           partial_lse, workspace, o, lse, counters, kv_page_indptr_host, s, &pk);
+                           partial_lse, workspace, o, lse, counters, kv_page_indptr_host, s, &pk, fp8);
         if (rc != FD_OK)
             return rc;
     }
@@ -429,6 +467,61 @@ extern "C" int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, in
     p.kv_last_len = kv_last_page_len_dev;
     p.page_size = page_size;
     return fd::launch_merge(p, s) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int fd_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                         const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+                         const void *q, const void *k, const void *v, float scale, float *o,
+                         float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    return decode_ragged(batch, num_qo_heads, num_kv_heads, head_dim, kv_indptr_host, kv_indptr_dev,
+                         q, k, v, scale, o, lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int fd_decode_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                             const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+                             const void *q, const void *k_fp8, const void *v_fp8,
+                             const float *k_scale, const float *v_scale, float scale, float *o,
+                             float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    const Fp8KV f{k_scale, v_scale};
+    return decode_ragged(batch, num_qo_heads, num_kv_heads, head_dim, kv_indptr_host, kv_indptr_dev,
+                         q, k_fp8, v_fp8, scale, o, lse, workspace, workspace_bytes, stream, &f);
+}
+
+extern "C" int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                               int page_size, int num_pages, const int32_t *kv_page_indptr_host,
+                               const int32_t *kv_last_page_len_host,
+                               const int32_t *kv_page_indptr_dev,
+                               const int32_t *kv_last_page_len_dev,
+                               const int32_t *kv_page_indices_dev, const void *q,
+                               const void *k_pages, const void *v_pages, float scale, float *o,
+                               float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    return decode_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
+                        kv_page_indptr_host, kv_last_page_len_host, kv_page_indptr_dev,
+                        kv_last_page_len_dev, kv_page_indices_dev, q, k_pages, v_pages, scale, o,
+                        lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                   int page_size, int num_pages, const int32_t *kv_page_indptr_host,
+                                   const int32_t *kv_last_page_len_host,
+                                   const int32_t *kv_page_indptr_dev,
+                                   const int32_t *kv_last_page_len_dev,
+                                   const int32_t *kv_page_indices_dev, const void *q,
+                                   const void *k_pages_fp8, const void *v_pages_fp8,
+                                   const float *k_scale, const float *v_scale, float scale,
+                                   float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                                   void *stream)
+{
+    const Fp8KV f{k_scale, v_scale};
+    return decode_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
+                        kv_page_indptr_host, kv_last_page_len_host, kv_page_indptr_dev,
+                        kv_last_page_len_dev, kv_page_indices_dev, q, k_pages_fp8, v_pages_fp8,
+                        scale, o, lse, workspace, workspace_bytes, stream, &f);
 }
 
 extern "C" int fd_get_device_status(void *workspace, void *stream)

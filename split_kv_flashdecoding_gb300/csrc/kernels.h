@@ -48,6 +48,11 @@ struct SplitParams {
     int32_t num_pages;
     int32_t num_page_entries;   // kv_indptr[B]
     int32_t last_len_param[kParamIndptr];
+    // FP8 (E4M3) K/V: one byte per element, dequantised in registers; k_scale,
+    // v_scale [Hkv] (device) multiply the head's K and V values.
+    int32_t kv_fp8;
+    const float *k_scale;
+    const float *v_scale;
 };
 
 struct MergeParams {
@@ -72,6 +77,10 @@ struct MergeParams {
 // that grid before touching global memory).
 cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
                          int group, int num_ctas, cudaStream_t stream);
+
+// The same for FP8 K/V (p.kv_fp8 set); launch_split dispatches to it.
+cudaError_t launch_split_fp8(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
+                             int group, int num_ctas, cudaStream_t stream);
 
 // Resident split-kernel CTAs per SM the launch shape is built for.
 int split_ctas_per_sm();

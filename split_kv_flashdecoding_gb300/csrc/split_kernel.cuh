@@ -1,0 +1,1456 @@
+// split_kernel.cuh -- stage 1 of split-KV decode attention on sm_103a (the
+// kernel templates; split_kernel.cu instantiates them for bf16 K/V and
+// split_kernel_fp8.cu for FP8 E4M3 K/V).
+//
+// "FlashDecoding++: sequence-dimension KV split parallelism for LLM serving"
+// (techknowgenie.com), §2 (each block keeps the query on chip and copies only
+// its own chunk of K/V from HBM into shared memory) and §3 stage 1 (per chunk:
+// logits, local max, exp, local sum, probability-weighted V; the block stores
+// the partial and exits).
+//
+// Work item = one (split, KV head).  All G query heads that share the KV head
+// are served from the same shared-memory tiles, so every K/V byte is read
+// from HBM once per step.  The kernel is persistent: a grid of at most
+// (SMs x resident CTAs per SM) CTAs, CTA c taking items c, c + grid, ... in
+// order.  Its tiles form one stream through the stage ring, so while the
+// consumer warps finish one item (combine, partial write, stage-2 ticket and
+// merge) the producer is already loading the next; a CTA's start-up and
+// epilogue costs are paid once per CTA rather than once per item.
+//
+// Warp roles:
+//   warp NC (producer): one lane issues TMA loads of 32-key tiles of K and V
+//     into an NS-stage ring guarded by full/empty mbarriers.  A tile is one
+//     3-D box per tensor holding both 64-column halves of the head's 32 rows
+//     (128-byte swizzle), or, for a paged cache whose pages are not a
+//     multiple of 32 keys, two such boxes of 16 rows.
+//     It hands each item to the consumers through a ring of kDescSlots
+//     descriptors (full/empty mbarriers of their own).
+//   warps 0..NC-1 (consumers): warp w takes stream tiles w, w+NC, ...  NS is a
+//     multiple of NC, so every stage always goes to the same warp and a warp
+//     never waits on a barrier more than one phase ahead (parity waits can only
+//     tell two phases apart).  Each warp keeps its own online-softmax state per
+//     item and at the item's end the NC states are merged in shared memory
+//     with the same rescaling as stage 2.
+//
+// Arithmetic per tile (warp-level mma.sync m16n8k16, bf16 in, fp32 accumulate):
+//   S = Q K^T    A = the G query rows (rows >= G are zero), kept in registers;
+//                B = K rows read with ldmatrix straight from the swizzled tile.
+//   online softmax on the fp32 accumulator fragments (base-2 logits: S is
+//                scaled by scale * log2 e; the running max and sum are per row).
+//   O += P V     A = P split into bf16 hi + lo parts: rows 0-7 carry hi, rows
+//                8-15 (padding in the score product) carry lo = P - hi, so the
+//                weights keep ~16 mantissa bits; O rows g and g+8 are added at
+//                the end.  B = V rows read with ldmatrix.trans.
+// The tensor cores are used here because the CUDA-core version of the same
+// loop was limited by shared-memory wavefronts (broadcast reads of q and p)
+// and instruction issue, not by HBM; the contraction itself stays tiny
+// (m = G <= 8 rows).
+#pragma once
+
+#include <cuda/atomic>
+#include <type_traits>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace fd {
+namespace {
+
+constexpr int kHalfBytes = kTile * 128;   // 32 keys x 64 bf16
+
+enum KvLayout { kKvRagged = 0, kKvPaged = 1, kKvPaged16 = 2 };
+enum KvType { kKvBf16 = 0, kKvFp8 = 1 };
+
+// One pipeline stage holds K then V for kTile = 32 keys of one KV head.
+//  bf16: a tensor's key row r (0..31), column half h (64 columns of 128 bytes,
+//    16-byte chunks XOR-swizzled by r % 8) sits at
+//      h * HalfStride + (r / 16) * BlockStride + (r % 16) * 128:
+//      ragged, paged:  [half][32 rows]            HalfStride 4096, BlockStride 2048
+//      paged16:        [16-row block][half][16]   HalfStride 2048, BlockStride 4096
+//    (paged16 is what one 16-row box of both halves per page lands as).
+//  FP8: a tensor is [32 rows][128 bytes] (a key row of the head is 128 one-byte
+//    values), 16-byte chunks XOR-swizzled by r % 8; a second 16-row page box
+//    lands 16 rows further.
+template <int KV, int DT>
+struct Stage {
+    static constexpr bool kFp8 = DT == kKvFp8;
+    static constexpr int kTensorBytes = kFp8 ? kTile * 128 : 2 * kHalfBytes;
+    static constexpr int kBytes = 2 * kTensorBytes;
+    static constexpr int kBoxRows = KV == kKvPaged16 ? 16 : kTile;
+    static constexpr int kHalfStride = KV == kKvPaged16 ? 2048 : kHalfBytes;
+    static constexpr int kBlockStride = KV == kKvPaged16 ? 4096 : 2048;
+};
+constexpr int kMaxGroup = 8;                   // rows 8-15 of the MMA carry the lo part of P
+
+enum Misc { kAbort, kIssued, kDescs, kLast, kFinalK, kMiscCount };
+
+// An item (one split of one KV head) as the producer hands it to the other
+// warps: request, its split prefix and count, split, key range [t0, t1)
+// relative to the request's first key, KV head, index of the item's first
+// tile in the CTA's stream of tiles, the head's K and V scales (FP8 K/V; float
+// bits), and a state: kItemOk, kItemBad (outside
+// the plan: the CTA stops) or kItemEnd (no further item; the previous one was
+// the CTA's last).
+enum Desc { kDB, kDPrefix, kDSplits, kDS, kDT0, kDT1, kDKvh, kDGt0, kDState, kDKs, kDVs, kDescInts };
+enum ItemState { kItemBad = 0, kItemOk = 1, kItemEnd = 2 };
+constexpr int kDescSlots = 4;
+
+struct Item {
+    int32_t b, prefix, splits, s, t0, t1, kvh, gt0, state, ks, vs;
+};
+
+__device__ __forceinline__ Item read_item(const volatile int *d)
+{
+    return Item{d[kDB], d[kDPrefix], d[kDSplits], d[kDS], d[kDT0], d[kDT1],
+                d[kDKvh], d[kDGt0], d[kDState], d[kDKs], d[kDVs]};
+}
+
+// Shared memory of the one-item kernel: [stage ring | full[NS] empty[NS] |
+// item descriptor | misc].  The consumer-state combine and the stage-2 merge
+// of the CTA's item work over the drained ring.
+template <int G, int NC, int NS, int SB>
+struct SingleLayout {
+    static_assert(NS % NC == 0, "each stage must belong to one consumer warp");
+    static_assert(G >= 1 && G <= kMaxGroup, "group size");
+    static constexpr int kWarps = NC + 1;
+    static_assert(kWarps * G * (kHeadDim + 2) * 4 <= NS * SB, "the merge fits the ring");
+    static constexpr int kOffBar = NS * SB;
+    static constexpr int kOffDesc = kOffBar + 2 * NS * 8;
+    static constexpr int kOffMisc = kOffDesc + kDescInts * 4;
+    static constexpr int kBytes = kOffMisc + kMiscCount * 4;
+    static constexpr int kAlloc = kBytes + 1024;   // room to align the base to 1024 B
+};
+
+// Shared memory of the persistent kernel (warps: 0..NC-1 consumers, NC
+// producer, NC+1 epilogue): [stage ring | Q of each item slot | 2 consumer-
+// state buffers | mbarriers | item descriptors | misc].  Barriers: full[NS],
+// empty[NS] (stages), item_full[4] (descriptor written and its Q landed),
+// item_empty[4] (consumers and epilogue warp are done with the slot),
+// state_full[2], state_empty[2] (a finished item's consumer states, handed to
+// the epilogue warp).
+template <int G, int NC, int NS, int SB>
+struct PersistentLayout {
+    static_assert(NS % NC == 0, "each stage must belong to one consumer warp");
+    static_assert(G >= 1 && G <= kMaxGroup, "group size");
+    static constexpr int kWarps = NC + 2;
+    static constexpr int kQBytes = G * kHeadDim * 2;                    // the item's G query rows
+    static constexpr int kQSlot = (kQBytes + 127) / 128 * 128;
+    static constexpr int kStateBytes = NC * G * (kHeadDim + 2) * 4;     // [NC][G][128] acc, m, l
+    static_assert(kWarps * G * (kHeadDim + 2) * 4 <= NS * SB,
+                  "the last item's merge works over the drained ring");
+    static constexpr int kOffQ = NS * SB;
+    static constexpr int kOffState = kOffQ + kDescSlots * kQSlot;
+    static constexpr int kOffBar = kOffState + 2 * kStateBytes;
+    static constexpr int kNumBars = 2 * NS + 2 * kDescSlots + 4;
+    static constexpr int kOffDesc = kOffBar + kNumBars * 8;
+    static constexpr int kOffMisc = kOffDesc + kDescSlots * kDescInts * 4;
+    static constexpr int kBytes = kOffMisc + kMiscCount * 4;
+    static constexpr int kAlloc = kBytes + 1024;   // room to align the base to 1024 B
+    static_assert(kOffBar % 8 == 0, "mbarriers are 8-byte aligned");
+};
+
+// Barrier of a group: BAR 0 = the whole CTA (__syncthreads), BAR -1 = one warp.
+template <int BAR>
+__device__ __forceinline__ void group_sync()
+{
+    static_assert(BAR == 0 || BAR == -1, "barrier");
+    if constexpr (BAR == 0)
+        __syncthreads();
+    else
+        __syncwarp();
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D (+)= A B for one m16n8k16 tile, bf16 inputs, fp32 accumulator.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D (+)= A B for one m16n8k16 tile, f16 inputs, fp32 accumulator.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> packed f16x2 (first argument in the low half), round to nearest.
+__device__ __forceinline__ uint32_t pack_f16(float lo_elem, float hi_elem)
+{
+    const __half2 h = __floats2half2_rn(lo_elem, hi_elem);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float f16_round(float x)
+{
+    return __half2float(__float2half_rn(x));
+}
+
+// Two E4M3 values in the low 16 bits of x (low byte first) -> f16x2 (low
+// byte in the low half).  Every E4M3 value is an f16 value, so this is exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x)
+{
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Two floats -> packed bf16x2 (first argument in the low half), round to nearest.
+__device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo_elem, hi_elem);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float bf16_round(float x)
+{
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Stage 2 for one (request, KV head) group, run by the CTA that finished the
+// group last: for each of its G heads, M = max_i LSE_i, w_i = exp(LSE_i - M),
+// O = sum_i w_i O_i / sum_i w_i, LSE = M + ln sum_i w_i over the group's splits.
+// Warp w of the first NW warps takes splits w, w + NW, ... (U splits of loads
+// in flight per batch, lane = 4 output columns, all G heads), keeps a running
+// maximum per head, and the NW warp states are combined through `scratch`
+// behind barrier BAR (a single warp writes O / LSE from its registers).  The
+// other CTAs' partials are read through L2 (ld.global.cg).
+template <int G, int NW, int BAR>
+__device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, int splits, int b,
+                                            int kvh, int warp, int lane, float *scratch)
+{
+    constexpr int U = (16 / G) > 1 ? 16 / G : 1;   // splits per batch: 16 float4 in flight
+    float m[G], den[G];
+    float4 acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        den[g] = 0.f;
+        acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int64_t row0 = partial_row(prefix, p.num_qo_heads, kvh * G, splits, 0);
+    for (int s0 = warp; s0 < splits; s0 += NW * U) {
+        float l[U][G];
+        float4 v[U][G];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + u * NW;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                // rows of head kvh*G + g are splits apart
+                const int64_t row = row0 + (int64_t)g * splits + s;
+                if (s < splits) {
+                    l[u][g] = __ldcg(p.partial_lse + row);
+                    v[u][g] = __ldcg(reinterpret_cast<const float4 *>(p.partial_o + row * kHeadDim) + lane);
+                } else {
+                    l[u][g] = -INFINITY;
+                    v[u][g] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float bm = l[0][g];
+#pragma unroll
+            for (int u = 1; u < U; ++u)
+                bm = fmaxf(bm, l[u][g]);
+            const float m_new = fmaxf(m[g], bm);
+            if (m_new == -INFINITY)   // only empty partials so far (none in practice)
+                continue;
+            const float f = expf(m[g] - m_new);
+            den[g] *= f;
+            acc[g].x *= f;
+            acc[g].y *= f;
+            acc[g].z *= f;
+            acc[g].w *= f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float w = expf(l[u][g] - m_new);
+                den[g] += w;
+                acc[g].x = fmaf(w, v[u][g].x, acc[g].x);
+                acc[g].y = fmaf(w, v[u][g].y, acc[g].y);
+                acc[g].z = fmaf(w, v[u][g].z, acc[g].z);
+                acc[g].w = fmaf(w, v[u][g].w, acc[g].w);
+            }
+            m[g] = m_new;
+        }
+    }
+    if constexpr (NW == 1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float inv = 1.f / den[g];
+            const int64_t row = (int64_t)b * p.num_qo_heads + kvh * G + g;
+            reinterpret_cast<float4 *>(p.o + row * kHeadDim)[lane] =
+                make_float4(acc[g].x * inv, acc[g].y * inv, acc[g].z * inv, acc[g].w * inv);
+            if (lane == 0)
+                p.lse[row] = m[g] + logf(den[g]);
+        }
+        return;
+    }
+    float *s_acc = scratch;                       // [NW][G][128]
+    float *s_m = scratch + NW * G * kHeadDim;     // [NW][G]
+    float *s_den = s_m + NW * G;                  // [NW][G]
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        reinterpret_cast<float4 *>(s_acc + (warp * G + g) * kHeadDim)[lane] = acc[g];
+        if (lane == 0) {
+            s_m[warp * G + g] = m[g];
+            s_den[warp * G + g] = den[g];
+        }
+    }
+    group_sync<BAR>();
+    for (int idx = warp * 32 + lane; idx < G * 32; idx += NW * 32) {
+        const int g = idx >> 5, c4 = idx & 31;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            mx = fmaxf(mx, s_m[w * G + g]);
+        float d = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = expf(s_m[w * G + g] - mx);   // 0 for a warp with no splits
+            d = fmaf(f, s_den[w * G + g], d);
+            const float4 t = reinterpret_cast<const float4 *>(s_acc + (w * G + g) * kHeadDim)[c4];
+            a.x = fmaf(f, t.x, a.x);
+            a.y = fmaf(f, t.y, a.y);
+            a.z = fmaf(f, t.z, a.z);
+            a.w = fmaf(f, t.w, a.w);
+        }
+        const float inv = 1.f / d;
+        const int64_t row = (int64_t)b * p.num_qo_heads + kvh * G + g;
+        reinterpret_cast<float4 *>(p.o + row * kHeadDim)[c4] =
+            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+        if (c4 == 0)
+            p.lse[row] = mx + logf(d);
+    }
+}
+
+// One consumer warp's work on one staged tile of 32 keys (stage at shared
+// address st, the first n_valid keys real): S = Q K^T on the tensor cores,
+// the online-softmax update of the running max m_run / row sum l_part (base 2,
+// logits = S * qk_scale), and O += P V.  qa: the Q fragments (A operand) of
+// the 8 k-steps of 16 head dimensions.
+//  bf16: mma.sync bf16; B fragments straight from the tile via ldmatrix.
+//  FP8: mma.sync f16; the E4M3 bytes are widened to f16 (exact) in registers.
+//    An ldmatrix of the 128-byte key rows read as 16-bit pairs gives lane
+//    (g, t4) dims 16c + 4t4 .. +3 of key g, which feed k positions 2t4, 2t4+1
+//    (dims +0, +1) and 2t4+8, 2t4+9 (dims +2, +3) of k-step c; qa holds q in the
+//    same order.  For P V, ldmatrix.trans gives lane (g, t4) dims 16c + 2g and
+//    +1 of keys 2t4 and 2t4+1, so one tile of columns takes the even dims and
+//    one the odd: o_acc[2c + e] holds dims 16c + 4t4 + e (and + 2).
+template <int KV, int DT>
+__device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uint32_t (&qa)[8][2],
+                                             float qk_scale, int lane, float &m_run, float &l_part,
+                                             float (&o_acc)[16][4])
+{
+    using S = Stage<KV, DT>;
+    const int t4 = lane & 3;
+    // ldmatrix: lane supplies row lr of matrix lm.  The 128-byte swizzle XORs
+    // the 16-byte chunk index with the row index mod 8, which is lr here.
+    const int lr = lane & 7, lm = lane >> 3;
+
+    // ---- S = Q K^T : 4 key groups (n-tiles) of 8, 8 k-steps of 16 dims
+    float sc[4][4];
+#pragma unroll
+    for (int jn = 0; jn < 4; ++jn)
+        sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
+    if constexpr (S::kFp8) {
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn) {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {         // chunks 4hc .. 4hc+3 (64 dims)
+                uint32_t kb[4];
+                ldsm_x4(st + (8 * jn + lr) * 128 + (((4 * hc + lm) ^ lr) << 4), kb);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int c = 4 * hc + m;
+                    mma_f16(sc[jn], qa[c][0], 0u, qa[c][1], 0u, e4m3x2_to_f16x2(kb[m]),
+                            e4m3x2_to_f16x2(kb[m] >> 16));
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {             // 32 columns per ldmatrix.x4
+            const uint32_t half = st + (kp >> 1) * S::kHalfStride;
+            const int chunk = 4 * (kp & 1) + lm;      // matrix lm = columns 8*lm .. +7
+#pragma unroll
+            for (int jn = 0; jn < 4; ++jn) {
+                // key row 8 jn + lr: block jn / 2, row 8 (jn % 2) + lr in it
+                const uint32_t row_off = (jn >> 1) * S::kBlockStride + (8 * (jn & 1) + lr) * 128;
+                uint32_t kb[4];
+                ldsm_x4(half + row_off + ((chunk ^ lr) << 4), kb);
+                mma_bf16(sc[jn], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, kb[0], kb[1]);
+                mma_bf16(sc[jn], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, kb[2], kb[3]);
+            }
+        }
+    }
+
+    // ---- online softmax on row g_row (this thread's 8 scores of the tile)
+    float x[8];
+    float mt = -INFINITY;
+#pragma unroll
+    for (int jn = 0; jn < 4; ++jn)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int key = 8 * jn + 2 * t4 + e;
+            const float v = key < n_valid ? sc[jn][e] * qk_scale : -INFINITY;
+            x[2 * jn + e] = v;
+            mt = fmaxf(mt, v);
+        }
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    const float m_new = fmaxf(m_run, mt);
+    const float alpha = exp2f(m_run - m_new);
+    m_run = m_new;
+    float psum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        x[e] = exp2f(x[e] - m_new);
+        psum += x[e];
+    }
+    l_part = fmaf(l_part, alpha, psum);
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            o_acc[n][0] *= alpha;
+            o_acc[n][1] *= alpha;
+            o_acc[n][2] *= alpha;
+            o_acc[n][3] *= alpha;
+        }
+    }
+    // P as the A operand: k-step ks covers keys 16ks .. 16ks+15 (n-tiles
+    // 2ks, 2ks+1); rows 0-7 hi, rows 8-15 lo = P - hi, in the MMA's type.
+    uint32_t pa[2][4];
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const float p0 = x[4 * ks], p1 = x[4 * ks + 1];
+        const float p2 = x[4 * ks + 2], p3 = x[4 * ks + 3];
+        if constexpr (S::kFp8) {
+            const float h0 = f16_round(p0), h1 = f16_round(p1);
+            const float h2 = f16_round(p2), h3 = f16_round(p3);
+            pa[ks][0] = pack_f16(h0, h1);
+            pa[ks][1] = pack_f16(p0 - h0, p1 - h1);
+            pa[ks][2] = pack_f16(h2, h3);
+            pa[ks][3] = pack_f16(p2 - h2, p3 - h3);
+        } else {
+            const float h0 = bf16_round(p0), h1 = bf16_round(p1);
+            const float h2 = bf16_round(p2), h3 = bf16_round(p3);
+            pa[ks][0] = pack_bf16(h0, h1);
+            pa[ks][1] = pack_bf16(p0 - h0, p1 - h1);
+            pa[ks][2] = pack_bf16(h2, h3);
+            pa[ks][3] = pack_bf16(p2 - h2, p3 - h3);
+        }
+    }
+
+    // ---- O += P V : 2 k-steps of 16 keys, 16 n-tiles of 8 columns
+    if constexpr (S::kFp8) {
+        const uint32_t vt = st + S::kTensorBytes;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            // matrix lm: keys 16 ks + 8 (lm & 1) .. +7, chunk 2 cp + (lm >> 1)
+            const uint32_t row = vt + (16 * ks + 8 * (lm & 1) + lr) * 128;
+#pragma unroll
+            for (int cp = 0; cp < 4; ++cp) {
+                uint32_t vb[4];
+                ldsm_x4_trans(row + (((2 * cp + (lm >> 1)) ^ lr) << 4), vb);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {         // chunk c = 2 cp + h: vb[2h] keys +0..7, vb[2h+1] +8..15
+                    const int c = 2 * cp + h;
+                    // bytes of vb: key 2t4 (dim 2g, 2g+1), key 2t4+1 (dim 2g, 2g+1)
+                    const uint32_t lo_even = __byte_perm(vb[2 * h], 0u, 0x0020);
+                    const uint32_t hi_even = __byte_perm(vb[2 * h + 1], 0u, 0x0020);
+                    const uint32_t lo_odd = __byte_perm(vb[2 * h], 0u, 0x0031);
+                    const uint32_t hi_odd = __byte_perm(vb[2 * h + 1], 0u, 0x0031);
+                    mma_f16(o_acc[2 * c], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3],
+                            e4m3x2_to_f16x2(lo_even), e4m3x2_to_f16x2(hi_even));
+                    mma_f16(o_acc[2 * c + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3],
+                            e4m3x2_to_f16x2(lo_odd), e4m3x2_to_f16x2(hi_odd));
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            // matrix lm: keys 16 ks + 8 (lm & 1) + lr = block ks, row 8 (lm & 1) + lr
+            const uint32_t row_off = ks * S::kBlockStride + (8 * (lm & 1) + lr) * 128;
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {          // 16 columns per ldmatrix.x4
+                const uint32_t half = st + 2 * kHalfBytes + (np >> 2) * S::kHalfStride;
+                const int chunk = 2 * (np & 3) + (lm >> 1);   // columns 8*(lm>>1) ..
+                uint32_t vb[4];
+                ldsm_x4_trans(half + row_off + ((chunk ^ lr) << 4), vb);
+                mma_bf16(o_acc[2 * np], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], vb[0], vb[1]);
+                mma_bf16(o_acc[2 * np + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], vb[2],
+                         vb[3]);
+            }
+        }
+    }
+}
+
+// The producer warp's side of the stage ring, one item at a time: where each
+// tile's rows are (in K/V, or through the page table in the page pool) and
+// how a tile is put into a stage.  page_id, next_box_row and tile_rows are
+// warp-collective in the paged layout (the warp shares a window of page ids);
+// issue is lane 0's.
+template <int NS, int KV, int DT>
+struct TileSource {
+    using SL = Stage<KV, DT>;
+    static constexpr bool kPaged = KV != kKvRagged;
+    const SplitParams &p;
+    const CUtensorMap *tm_k, *tm_v;
+    uint8_t *ring;
+    uint64_t *full;   // full[NS]
+    uint64_t pol;
+    int lane;
+    int32_t t0 = 0, req_base = 0, req_pages = 0;
+    // paged: lane l holds the page id of page win_first + l, and nxt_id that
+    // of page win_first + 32 + l, loaded one window ahead so that moving on to
+    // the next window never waits for a global load.
+    int32_t win_first = 0, win_id = 0, nxt_id = 0;
+    // paged: the next box starts at row cur_off of the request's page cur_pg;
+    // the cursor only moves forward within an item.
+    int32_t cur_pg = 0, cur_off = 0;
+
+    __device__ __forceinline__ TileSource(const SplitParams &p_, const CUtensorMap *k,
+                                          const CUtensorMap *v, uint8_t *ring_, uint64_t *full_,
+                                          int lane_)
+        : p(p_), tm_k(k), tm_v(v), ring(ring_), full(full_), pol(l2_evict_first_policy()), lane(lane_)
+    {
+    }
+
+    // An item of keys t0.. (relative to its request's first key); base and
+    // pages locate the request (first key row, or first page-list entry).
+    __device__ __forceinline__ void begin_item(int32_t t0_, int32_t base, int32_t pages)
+    {
+        t0 = t0_;
+        req_base = base;
+        req_pages = pages;
+        if constexpr (kPaged) {
+            win_first = -(1 << 30);   // far below page 0: the first lookup fills the window
+            cur_pg = t0 / p.page_size;
+            cur_off = t0 % p.page_size;
+        }
+    }
+
+    __device__ __forceinline__ int32_t fetch_ids(int32_t first) const
+    {
+        return first + lane < req_pages ? __ldg(p.page_indices + req_base + first + lane) : 0;
+    }
+
+    // Physical page of the request's page `pg`; a page outside the pool is
+    // reported (FD_ERR_DEVICE_BOUNDS) and page 0 read instead.
+    __device__ __forceinline__ int32_t page_id(int32_t pg)
+    {
+        if (pg < win_first || pg >= win_first + 32) {
+            win_id = pg == win_first + 32 ? nxt_id : fetch_ids(pg);
+            win_first = pg;
+            nxt_id = fetch_ids(pg + 32);
+        }
+        int32_t id = __shfl_sync(0xffffffffu, win_id, pg - win_first);
+        if (id < 0 || id >= p.num_pages) {
+            if (lane == 0)
+                report(p.status, FD_ERR_DEVICE_BOUNDS);
+            id = 0;
+        }
+        return id;
+    }
+
+    __device__ __forceinline__ int32_t next_box_row()
+    {
+        // Rows past the request's last key read whatever its last page holds
+        // there; the consumers mask them.
+        const int32_t y = page_id(min(cur_pg, req_pages - 1)) * p.page_size + cur_off;
+        cur_off += SL::kBoxRows;
+        if (cur_off >= p.page_size) {
+            cur_off -= p.page_size;
+            ++cur_pg;
+        }
+        return y;
+    }
+
+    // First rows (in K/V, or in the page pool) of the item's tile i: ya, and
+    // yb for the second 16-row box of a paged tile.  The producer computes them
+    // before it waits for the tile's stage, so that only the copies remain
+    // once the stage is free.
+    __device__ __forceinline__ void tile_rows(int i, int32_t &ya, int32_t &yb)
+    {
+        if constexpr (!kPaged) {
+            ya = req_base + t0 + i * kTile;
+        } else {
+            ya = next_box_row();
+            if constexpr (SL::kBoxRows < kTile)
+                yb = next_box_row();
+        }
+    }
+
+    // Put stream tile g (KV head kvh) into stage g % NS, per tensor and per box
+    // of rows: bf16, one 3-D box of both 64-column halves; FP8, one 2-D box of
+    // the rows' 128 bytes.
+    __device__ __forceinline__ void issue(int g, int kvh, int32_t ya, int32_t yb) const
+    {
+        const int s = g % NS;
+        const uint32_t bar = smem_addr(&full[s]);
+        const uint32_t dst = smem_addr(ring + s * SL::kBytes);
+        mbar_arrive_expect_tx(bar, SL::kBytes);
+        if constexpr (SL::kFp8) {
+            const int32_t x = kvh * kHeadDim;
+            tma_load_2d(dst, tm_k, x, ya, bar, pol);
+            tma_load_2d(dst + SL::kTensorBytes, tm_v, x, ya, bar, pol);
+            if constexpr (SL::kBoxRows < kTile) {
+                tma_load_2d(dst + 16 * 128, tm_k, x, yb, bar, pol);
+                tma_load_2d(dst + SL::kTensorBytes + 16 * 128, tm_v, x, yb, bar, pol);
+            }
+        } else {
+            tma_load_3d(dst, tm_k, 0, ya, 2 * kvh, bar, pol);
+            tma_load_3d(dst + SL::kTensorBytes, tm_v, 0, ya, 2 * kvh, bar, pol);
+            if constexpr (SL::kBoxRows < kTile) {
+                tma_load_3d(dst + SL::kBlockStride, tm_k, 0, yb, 2 * kvh, bar, pol);
+                tma_load_3d(dst + SL::kTensorBytes + SL::kBlockStride, tm_v, 0, yb, 2 * kvh, bar, pol);
+            }
+        }
+    }
+};
+
+// Locate split j of the plan (warp-collective) and check it against the
+// buffers: key range [t0, t1) relative to the request's first key.
+template <bool PAGED>
+__device__ __forceinline__ bool item_range(const SplitParams &p, const SplitCoord &c, bool found,
+                                           int32_t &t0, int32_t &t1)
+{
+    t0 = t1 = 0;
+    if (!found)
+        return false;
+    const int32_t len = split_len_for(c.len, c.splits);
+    t0 = c.s * len;
+    t1 = min(t0 + len, c.len);
+    return t0 < t1 && c.base >= 0 &&
+           (PAGED ? c.base + c.pages <= p.num_page_entries : c.base + c.len <= p.total_tokens) &&
+           partial_row(c.prefix, p.num_qo_heads, p.num_qo_heads - 1, c.splits, c.splits - 1) <
+               p.num_partial_rows;
+}
+
+__device__ __forceinline__ void write_desc(volatile int *d, const SplitCoord &c, int32_t t0,
+                                           int32_t t1, int kvh, int gt0, int state, float ks = 1.f,
+                                           float vs = 1.f)
+{
+    d[kDKs] = __float_as_int(ks);
+    d[kDVs] = __float_as_int(vs);
+    d[kDB] = c.b;
+    d[kDPrefix] = c.prefix;
+    d[kDSplits] = c.splits;
+    d[kDS] = c.s;
+    d[kDT0] = t0;
+    d[kDT1] = t1;
+    d[kDKvh] = kvh;
+    d[kDGt0] = gt0;
+    d[kDState] = state;
+}
+
+__device__ __forceinline__ KeyIndex key_index(const SplitParams &p, bool paged)
+{
+    return p.indptr_in_params ? KeyIndex{p.indptr_param, paged ? p.last_len_param : nullptr, p.page_size}
+                              : KeyIndex{p.kv_indptr, p.kv_last_len, p.page_size};
+}
+
+// Q fragments (A operand of S = Q K^T) for the 8 k-steps of 16 dims from the
+// G bf16 query rows at `qrows` (global or shared); rows g >= G and the padding
+// rows 8-15 are zero.  Returns the factor the logits must be multiplied by.
+//  bf16: qa[c] = dims 16c + 2t4 (+1) and 16c + 8 + 2t4 (+1), as stored; 1.
+//  FP8 (f16 MMA): qa[c] = dims 16c + 4t4 (+1) and 16c + 4t4 + 2 (+3), the order
+//    consume_tile reads K in.  Each row is first scaled by the power of two
+//    that puts its largest magnitude in [2^8, 2^9), so every bf16 value of the
+//    row converts to f16 exactly (values below 2^-22 of the row's maximum
+//    round in f16's subnormal range); returns the inverse power.
+template <int G, int DT, bool GLOBAL>
+__device__ __forceinline__ float load_q(const uint16_t *qrows, int lane, uint32_t (&qa)[8][2])
+{
+    const int g_row = lane >> 2, t4 = lane & 3;
+    const bool valid = g_row < G;
+    if constexpr (DT == kKvFp8) {
+        const uint2 *row = reinterpret_cast<const uint2 *>(qrows + (valid ? g_row : 0) * kHeadDim);
+        uint2 raw[8];
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if constexpr (GLOBAL)
+                raw[c] = valid ? __ldg(row + 4 * c + t4) : make_uint2(0u, 0u);
+            else
+                raw[c] = valid ? row[4 * c + t4] : make_uint2(0u, 0u);
+            const float2 a = bf16x2_to_float2(raw[c].x), b = bf16x2_to_float2(raw[c].y);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int sh = 0;
+        if (amax > 0.f) {
+            int e;
+            frexpf(amax, &e);   // amax in [2^(e-1), 2^e)
+            sh = min(max(9 - e, -100), 100);
+        }
+        const float up = __int_as_float((127 + sh) << 23);   // 2^sh, exact
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float2 a = bf16x2_to_float2(raw[c].x), b = bf16x2_to_float2(raw[c].y);
+            qa[c][0] = pack_f16(a.x * up, a.y * up);
+            qa[c][1] = pack_f16(b.x * up, b.y * up);
+        }
+        return __int_as_float((127 - sh) << 23);   // 2^-sh
+    } else {
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qrows) + (valid ? g_row : 0) * (kHeadDim / 2);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            if constexpr (GLOBAL) {
+                qa[kk][0] = valid ? __ldg(qrow + kk * 8 + t4) : 0u;       // cols 16kk + 2t4 (+1)
+                qa[kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + t4) : 0u;   // cols 16kk + 8 + 2t4 (+1)
+            } else {
+                qa[kk][0] = valid ? qrow[kk * 8 + t4] : 0u;
+                qa[kk][1] = valid ? qrow[kk * 8 + 4 + t4] : 0u;
+            }
+        }
+        return 1.f;
+    }
+}
+
+// Consumer warp `warp`: put its online-softmax state for one item (O rows g
+// and g+8 summed and multiplied by vscale, running max, row sum) into a state
+// buffer, O in dim order (consume_tile's FP8 column order is undone here).
+template <int G, int NC, int DT>
+__device__ __forceinline__ void write_state(uint8_t *state, int warp, int lane,
+                                            const float (&o_acc)[16][4], float m_run, float l_part,
+                                            float vscale)
+{
+    float *comb_acc = reinterpret_cast<float *>(state);
+    float *comb_m = comb_acc + NC * G * kHeadDim;
+    float *comb_l = comb_m + NC * G;
+    const int g_row = lane >> 2, t4 = lane & 3;
+    float l_tot = l_part;
+    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+    if (g_row < G) {
+        if constexpr (DT == kKvFp8) {
+            float *dst = comb_acc + (warp * G + g_row) * kHeadDim + 4 * t4;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)   // dims 16c + 4t4 + (0, 1, 2, 3)
+                *reinterpret_cast<float4 *>(dst + 16 * c) = make_float4(
+                    (o_acc[2 * c][0] + o_acc[2 * c][2]) * vscale,
+                    (o_acc[2 * c + 1][0] + o_acc[2 * c + 1][2]) * vscale,
+                    (o_acc[2 * c][1] + o_acc[2 * c][3]) * vscale,
+                    (o_acc[2 * c + 1][1] + o_acc[2 * c + 1][3]) * vscale);
+        } else {
+            float *dst = comb_acc + (warp * G + g_row) * kHeadDim + 2 * t4;
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                *reinterpret_cast<float2 *>(dst + 8 * n) =
+                    make_float2(o_acc[n][0] + o_acc[n][2], o_acc[n][1] + o_acc[n][3]);
+        }
+        if (t4 == 0) {
+            comb_m[warp * G + g_row] = m_run;
+            comb_l[warp * G + g_row] = l_tot;
+        }
+    }
+}
+
+// End of one item, run by NW warps (thread `tid` of NW * 32) behind barrier
+// BAR: NW = 1, BAR = -1 is the epilogue warp while the others stream the next
+// items; NW = all warps, BAR = 0 is the whole CTA after its last item.
+// Combines the NC consumer states in `state` into the item's normalised
+// partial -- or O / LSE directly when stage 2 is fused and the request has one
+// split -- calls combined() once the state buffer has been read, then takes
+// the group's ticket and, as the group's last CTA, runs stage 2 (using
+// `merge_scratch` when NW > 1).
+template <int G, int NC, int NW, int BAR, typename Combined>
+__device__ __forceinline__ void finish_item(const SplitParams &p, const Item &it, const uint8_t *state,
+                                            uint8_t *merge_scratch, volatile int *misc, int tid,
+                                            Combined combined)
+{
+    const float *comb_acc = reinterpret_cast<const float *>(state);
+    const float *comb_m = comb_acc + NC * G * kHeadDim;
+    const float *comb_l = comb_m + NC * G;
+    const bool direct = p.fuse_merge && it.splits == 1;
+    for (int idx = tid; idx < G * 32; idx += NW * 32) {
+        const int g = idx >> 5, c4 = idx & 31;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NC; ++w)
+            mx = fmaxf(mx, comb_m[w * G + g]);
+        float den = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+            const float e = mx == -INFINITY ? 0.f : exp2f(comb_m[w * G + g] - mx);
+            den = fmaf(e, comb_l[w * G + g], den);
+            const float4 a = *reinterpret_cast<const float4 *>(comb_acc + (w * G + g) * kHeadDim + 4 * c4);
+            o.x = fmaf(e, a.x, o.x);
+            o.y = fmaf(e, a.y, o.y);
+            o.z = fmaf(e, a.z, o.z);
+            o.w = fmaf(e, a.w, o.w);
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        o.x *= inv;
+        o.y *= inv;
+        o.z *= inv;
+        o.w *= inv;
+        const float lse_nat = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+        if (direct) {
+            const int64_t row = (int64_t)it.b * p.num_qo_heads + it.kvh * G + g;
+            *reinterpret_cast<float4 *>(p.o + row * kHeadDim + 4 * c4) = o;
+            if (c4 == 0)
+                p.lse[row] = lse_nat;
+        } else {
+            const int64_t row = partial_row(it.prefix, p.num_qo_heads, it.kvh * G + g, it.splits, it.s);
+            *reinterpret_cast<float4 *>(p.partial_o + row * kHeadDim + 4 * c4) = o;
+            if (c4 == 0)
+                p.partial_lse[row] = lse_nat;
+        }
+    }
+    combined();
+
+    if (p.fuse_merge && it.splits > 1) {
+        // Ticket: the last CTA of the (request, KV head) group to finish merges
+        // the group (stage 2).  The ticket add is acquire-release at GPU scope:
+        // it publishes this item's partials (made visible to thread 0 by the
+        // barrier) and lets the last CTA see everyone else's; that CTA also
+        // resets the ticket for the next call.
+        group_sync<BAR>();
+        if (tid == 0) {
+            cuda::atomic_ref<int, cuda::thread_scope_device> ticket(
+                p.counters[(int64_t)it.b * p.num_kv_heads + it.kvh]);
+            const int prev = ticket.fetch_add(1, cuda::memory_order_acq_rel);
+            const bool last = prev == it.splits - 1;
+            if (last)
+                ticket.store(0, cuda::memory_order_relaxed);
+            misc[kLast] = last;
+        }
+        group_sync<BAR>();
+        if (misc[kLast])
+            merge_group<G, NW, BAR>(p, it.prefix, it.splits, it.b, it.kvh, tid >> 5, tid & 31,
+                                    reinterpret_cast<float *>(merge_scratch));
+    }
+    group_sync<BAR>();
+}
+
+// One item per CTA: the grid is the items, all resident at once (the plan
+// fits one wave).  Warp NC produces, warps 0..NC-1 consume, and the whole CTA
+// closes the item.
+template <int G, int NC, int NS, int MIN_CTAS, int KV, int DT>
+__global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
+    split_kv_kernel(const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ SplitParams p)
+{
+    using SG = Stage<KV, DT>;
+    using L = SingleLayout<G, NC, NS, SG::kBytes>;
+    constexpr bool paged = KV != kKvRagged;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
+    volatile int *desc = reinterpret_cast<volatile int *>(smem + L::kOffDesc);
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + L::kOffMisc);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kvh = blockIdx.x % p.num_kv_heads;
+    // The inputs may come from the preceding grid in the stream: wait for it
+    // before touching global memory (the launch itself overlaps its tail).
+    // When kv_indptr is in the launch parameters, the producer warp locates
+    // its split before that wait.
+    const bool early_derive = p.indptr_in_params && warp == NC;
+    if (!early_derive)
+        griddep_wait();
+
+    float m_run = -INFINITY, l_part = 0.f, vscale = 1.f;
+    float o_acc[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+        o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+
+    if (warp == NC) {
+        // ---------------------------------------------------------- producer
+        // Locate the split (the host planner's rule), set up the barriers and
+        // put the first NS tiles in flight before the CTA barrier.  With the
+        // paged layout the whole warp runs the issue loop; lane 0 issues the
+        // barrier operations and the copies.
+        SplitCoord c{};
+        const bool found = derive_split(key_index(p, paged), p.batch, p.chunk,
+                                        blockIdx.x / p.num_kv_heads, false, c);
+        if (early_derive)
+            griddep_wait();
+        int32_t t0, t1;
+        const bool ok = item_range<paged>(p, c, found, t0, t1);
+        if (lane == 0) {
+            write_desc(desc, c, t0, t1, kvh, 0, ok ? kItemOk : kItemBad);
+            misc[kAbort] = ok ? 0 : 1;
+            misc[kIssued] = 0;
+            misc[kLast] = 0;
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(smem_addr(&bars[s]), 1);        // full: producer arrive + TMA bytes
+                mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: the stage's consumer warp
+            }
+            fence_mbar_init();
+            if (!ok)
+                report(p.status, FD_ERR_DEVICE_BOUNDS);
+        }
+        __syncwarp();
+        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
+        const int n_tiles = ok ? (t1 - t0 + kTile - 1) / kTile : 0;
+        const int first = min(NS, n_tiles);
+        if (ok && (paged || lane == 0)) {
+            src.begin_item(t0, c.base, c.pages);
+            for (int i = 0; i < first; ++i) {
+                int32_t ya = 0, yb = 0;
+                src.tile_rows(i, ya, yb);
+                if (lane == 0)
+                    src.issue(i, kvh, ya, yb);
+            }
+        }
+        if (lane == 0)
+            misc[kIssued] = first;
+        __syncthreads();   // the barriers are initialised
+        if (ok && (paged || lane == 0)) {
+            int issued = first;
+            for (int i = first; i < n_tiles; ++i) {
+                int32_t ya = 0, yb = 0;
+                src.tile_rows(i, ya, yb);
+                int go = 0;
+                if (lane == 0) {
+                    go = mbar_wait(smem_addr(&bars[NS + i % NS]), ((i / NS) - 1) & 1, p.timeout_ns);
+                    if (!go) {
+                        misc[kAbort] = 1;
+                        report(p.status, FD_ERR_TIMEOUT);
+                    } else if (misc[kAbort]) {
+                        go = 0;
+                    }
+                    if (go)
+                        src.issue(i, kvh, ya, yb);
+                }
+                if constexpr (paged)
+                    go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go)
+                    break;
+                issued = i + 1;
+            }
+            if (lane == 0)
+                misc[kIssued] = issued;
+        }
+    } else {
+        // ---------------------------------------------------------- consumers
+        __syncthreads();   // the barriers are initialised
+        const Item it = read_item(desc);
+        if (it.state == kItemOk) {
+            uint32_t qa[8][2];
+            float qk = p.q_scale *
+                       load_q<G, DT, true>(p.q + ((int64_t)it.b * p.num_qo_heads + kvh * G) * kHeadDim,
+                                           lane, qa);
+            if constexpr (DT == kKvFp8) {   // the head's dequantisation scales
+                qk *= __ldg(p.k_scale + kvh);
+                vscale = __ldg(p.v_scale + kvh);
+            }
+            const uint32_t ring = smem_addr(smem);
+            const int n_tiles = (it.t1 - it.t0 + kTile - 1) / kTile;
+            for (int i = warp; i < n_tiles; i += NC) {
+                const int s = i % NS;
+                if (!mbar_wait(smem_addr(&bars[s]), (i / NS) & 1, p.timeout_ns)) {
+                    misc[kAbort] = 1;
+                    if (lane == 0)
+                        report(p.status, FD_ERR_TIMEOUT);
+                    break;
+                }
+                consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
+                                     qk, lane, m_run, l_part, o_acc);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&bars[NS + s]));
+            }
+        }
+    }
+
+    __syncthreads();
+    if (misc[kAbort]) {
+        // Let every copy this CTA issued land before the CTA exits.
+        if (warp == NC && lane == 0) {
+            const int issued = misc[kIssued];
+            for (int i = max(0, issued - NS); i < issued; ++i)
+                if (!mbar_wait(smem_addr(&bars[i % NS]), (i / NS) & 1, kDrainTimeoutNs))
+                    report(p.status, FD_ERR_TIMEOUT);
+        }
+        __syncthreads();
+        return;
+    }
+    // ---- close the item: consumer states over the drained ring, then the
+    // whole CTA combines them (and runs stage 2 as the group's last CTA)
+    if (warp < NC)
+        write_state<G, NC, DT>(smem, warp, lane, o_acc, m_run, l_part, vscale);
+    __syncthreads();
+    finish_item<G, NC, NC + 1, 0>(p, read_item(desc), smem, smem, misc, tid, [] {});
+    // This CTA's outputs are written: a dependent grid may launch.
+    griddep_launch_dependents();
+}
+
+// Persistent (the plan needs more than one wave): at most one wave of resident
+// CTAs.  CTA c starts with item c (item w = split w / Hkv of KV head w % Hkv,
+// the planner's order) and then claims its next items from a counter, one item
+// ahead so that the claim's latency hides behind the current item; that keeps
+// a ragged batch balanced the way block scheduling would.  A CTA's tiles form
+// one stream through the stage ring: the producer loads the next item while
+// the consumers finish the current one and the epilogue warp closes the one
+// before (combine, partial write, ticket, stage 2 as the group's last CTA);
+// the CTA's last item is closed by the whole CTA.
+template <int G, int NC, int NS, int MIN_CTAS, int KV, int DT>
+__global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
+    split_kv_persistent_kernel(const __grid_constant__ CUtensorMap tm_k,
+                               const __grid_constant__ CUtensorMap tm_v,
+                               const __grid_constant__ SplitParams p)
+{
+    using SG = Stage<KV, DT>;
+    using L = PersistentLayout<G, NC, NS, SG::kBytes>;
+    constexpr bool paged = KV != kKvRagged;
+    constexpr int kProducer = NC;   // the epilogue warp is NC + 1
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *qslots = smem + L::kOffQ;
+    uint8_t *states = smem + L::kOffState;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
+    uint64_t *item_full = bars + 2 * NS;
+    uint64_t *item_empty = item_full + kDescSlots;
+    uint64_t *state_full = item_empty + kDescSlots;
+    uint64_t *state_empty = state_full + 2;
+    volatile int *desc = reinterpret_cast<volatile int *>(smem + L::kOffDesc);
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + L::kOffMisc);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t grid = (int32_t)gridDim.x;
+    const bool early_derive = p.indptr_in_params && warp == kProducer;
+    if (!early_derive)
+        griddep_wait();
+
+    if (warp == kProducer) {
+        // ---------------------------------------------------------- producer
+        // The whole warp locates each item (and, paged, runs the issue loop);
+        // lane 0 issues the barrier operations, the claims and the copies.  It
+        // sets up the barriers and puts the first tiles in flight before the
+        // CTA barrier.
+        if (lane == 0) {
+            misc[kAbort] = 0;
+            misc[kIssued] = 0;
+            misc[kDescs] = 0;
+            misc[kLast] = 0;
+            misc[kFinalK] = 0;
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(smem_addr(&bars[s]), 1);        // full: producer arrive + TMA bytes
+                mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: the stage's consumer warp
+            }
+            for (int s = 0; s < kDescSlots; ++s) {
+                mbar_init(smem_addr(&item_full[s]), 1);        // producer arrive (+ Q bytes)
+                mbar_init(smem_addr(&item_empty[s]), NC + 1);  // consumer warps + epilogue warp
+            }
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(smem_addr(&state_full[s]), NC);   // every consumer warp wrote its state
+                mbar_init(smem_addr(&state_empty[s]), 1);   // the epilogue warp read it
+            }
+            fence_mbar_init();
+        }
+        __syncwarp();
+        bool synced = false;
+        auto cta_sync = [&]() {
+            if (!synced) {
+                __syncthreads();   // the barriers are initialised
+                synced = true;
+            }
+        };
+        const KeyIndex ki = key_index(p, paged);
+        SplitCursor cursor;
+        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
+        int gt = 0;      // tiles issued so far (index of the stream's next tile)
+        int descs = 0;   // descriptors published (lane 0)
+
+        // Issue the item's tiles i0 .. i1-1 (stream tiles from gt on); false if
+        // the CTA stops (a wait ran out, or another warp gave up).
+        auto issue_range = [&](int i0, int i1, int kvh) -> bool {
+            int stop = 0;
+            if (paged || lane == 0) {
+                for (int i = i0; i < i1; ++i) {
+                    int32_t ya = 0, yb = 0;
+                    src.tile_rows(i, ya, yb);
+                    int go = 0;
+                    if (lane == 0) {
+                        go = gt < NS ? 1
+                                     : mbar_wait(smem_addr(&bars[NS + gt % NS]), ((gt / NS) - 1) & 1,
+                                                 p.timeout_ns);
+                        if (!go) {
+                            misc[kAbort] = 1;
+                            report(p.status, FD_ERR_TIMEOUT);
+                        } else if (misc[kAbort]) {
+                            go = 0;
+                        }
+                        if (go)
+                            src.issue(gt, kvh, ya, yb);
+                    }
+                    if constexpr (paged)
+                        go = __shfl_sync(0xffffffffu, go, 0);
+                    if (!go) {
+                        stop = 1;
+                        break;
+                    }
+                    ++gt;
+                }
+            }
+            stop = __shfl_sync(0xffffffffu, stop, 0);
+            gt = __shfl_sync(0xffffffffu, gt, 0);
+            return !stop;
+        };
+        // Lane 0: wait until descriptor slot k's previous item is closed;
+        // false if the CTA stops.
+        auto slot_free = [&](int k) -> bool {
+            int go = 1;
+            if (k >= kDescSlots)
+                go = mbar_wait(smem_addr(&item_empty[k % kDescSlots]), ((k / kDescSlots) - 1) & 1,
+                               p.timeout_ns);
+            if (!go) {
+                misc[kAbort] = 1;
+                report(p.status, FD_ERR_TIMEOUT);
+            } else if (misc[kAbort]) {
+                go = 0;
+            }
+            return go;
+        };
+
+        int k = 0;
+        int32_t w = blockIdx.x;     // this item
+        int32_t nxt = p.num_work;   // the CTA's next item (lane 0; claimed during this one)
+        for (;;) {
+            const int kvh = w % p.num_kv_heads;
+            SplitCoord c{};
+            const bool found = cursor.find(ki, p.batch, p.chunk, w / p.num_kv_heads, c);
+            if (k == 0 && early_derive)
+                griddep_wait();
+            if (lane == 0)
+                nxt = grid + atomicAdd(p.claim, 1);
+            int32_t t0, t1;
+            const bool ok = item_range<paged>(p, c, found, t0, t1);
+            // hand the item (descriptor + its Q rows) to the other warps
+            const int slot = k % kDescSlots;
+            int go = 0;
+            if (lane == 0) {
+                go = slot_free(k);
+                if (go) {
+                    float ks = 1.f, vs = 1.f;
+                    if constexpr (DT == kKvFp8) {   // the head's dequantisation scales
+                        ks = __ldg(p.k_scale + kvh);
+                        vs = __ldg(p.v_scale + kvh);
+                    }
+                    write_desc(desc + slot * kDescInts, c, t0, t1, kvh, gt, ok ? kItemOk : kItemBad,
+                               ks, vs);
+                    ++descs;
+                    const uint32_t fb = smem_addr(&item_full[slot]);
+                    if (ok) {
+                        mbar_arrive_expect_tx(fb, L::kQBytes);
+                        bulk_load(smem_addr(qslots + slot * L::kQSlot),
+                                  p.q + ((int64_t)c.b * p.num_qo_heads + kvh * G) * kHeadDim,
+                                  L::kQBytes, fb);
+                    } else {
+                        report(p.status, FD_ERR_DEVICE_BOUNDS);
+                        misc[kAbort] = 1;
+                        mbar_arrive(fb);
+                    }
+                }
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go || !ok)
+                break;
+            src.begin_item(t0, c.base, c.pages);
+            const int n_tiles = (t1 - t0 + kTile - 1) / kTile;
+            const int first = k == 0 ? min(NS, n_tiles) : n_tiles;
+            if (!issue_range(0, first, kvh))
+                break;
+            cta_sync();
+            if (!issue_range(first, n_tiles, kvh))
+                break;
+            // the next item, or the end of the CTA's stream
+            w = __shfl_sync(0xffffffffu, nxt, 0);
+            ++k;
+            if (w >= p.num_work) {
+                if (lane == 0) {
+                    // the claim that returned num_work - 1 was the grid's last one
+                    if (nxt - grid == p.num_work - 1)
+                        atomicExch(p.claim, 0);
+                    if (slot_free(k)) {
+                        desc[(k % kDescSlots) * kDescInts + kDState] = kItemEnd;
+                        ++descs;
+                        mbar_arrive(smem_addr(&item_full[k % kDescSlots]));
+                    }
+                }
+                break;
+            }
+        }
+        cta_sync();
+        if (lane == 0) {
+            misc[kIssued] = gt;
+            misc[kDescs] = descs;
+        }
+    } else if (warp < NC) {
+        // ---------------------------------------------------------- consumers
+        __syncthreads();   // the barriers are initialised
+        const uint32_t ring = smem_addr(smem);
+        int k = 0;
+        bool ok = mbar_wait(smem_addr(&item_full[0]), 0, p.timeout_ns);
+        if (!ok) {
+            misc[kAbort] = 1;
+            if (lane == 0)
+                report(p.status, FD_ERR_TIMEOUT);
+        }
+        Item it = read_item(desc);
+        while (ok && it.state == kItemOk) {
+            const int slot = k % kDescSlots;
+            float m_run = -INFINITY, l_part = 0.f;
+            float o_acc[16][4];
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+            uint32_t qa[8][2];
+            const float qk = p.q_scale * __int_as_float(it.ks) *
+                             load_q<G, DT, false>(reinterpret_cast<const uint16_t *>(qslots + slot * L::kQSlot),
+                                                  lane, qa);
+            const int n_tiles = (it.t1 - it.t0 + kTile - 1) / kTile;
+            // this warp's tiles of the item: stream tiles g = warp (mod NC)
+            const int first = it.gt0 + ((warp - it.gt0 % NC) + NC) % NC;
+            for (int g = first; g < it.gt0 + n_tiles; g += NC) {
+                const int i = g - it.gt0;
+                const int s = g % NS;
+                if (!mbar_wait(smem_addr(&bars[s]), (g / NS) & 1, p.timeout_ns)) {
+                    misc[kAbort] = 1;
+                    if (lane == 0)
+                        report(p.status, FD_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
+                                     qk, lane, m_run, l_part, o_acc);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&bars[NS + s]));
+            }
+            if (!ok)
+                break;
+            // The next descriptor tells whether this was the CTA's last item.
+            const int nslot = (k + 1) % kDescSlots;
+            ok = mbar_wait(smem_addr(&item_full[nslot]), ((k + 1) / kDescSlots) & 1, p.timeout_ns);
+            if (!ok) {
+                misc[kAbort] = 1;
+                if (lane == 0)
+                    report(p.status, FD_ERR_TIMEOUT);
+                break;
+            }
+            const Item nx = read_item(desc + nslot * kDescInts);
+            // state buffer k % 2: the epilogue warp must have read item k - 2's
+            const int sb = k & 1;
+            if (k >= 2 && !mbar_wait(smem_addr(&state_empty[sb]), ((k >> 1) - 1) & 1, p.timeout_ns)) {
+                misc[kAbort] = 1;
+                if (lane == 0)
+                    report(p.status, FD_ERR_TIMEOUT);
+                break;
+            }
+            write_state<G, NC, DT>(states + sb * L::kStateBytes, warp, lane, o_acc, m_run, l_part,
+                                   __int_as_float(it.vs));
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&state_full[sb]));
+            if (nx.state != kItemOk) {
+                // the CTA's last item: the whole CTA closes it below
+                if (warp == 0 && lane == 0)
+                    misc[kFinalK] = k;
+                break;
+            }
+            if (lane == 0)
+                mbar_arrive(smem_addr(&item_empty[slot]));
+            it = nx;
+            ++k;
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        // Closes every item but the CTA's last while the other warps stream on.
+        __syncthreads();   // the barriers are initialised
+        for (int k = 0;; ++k) {
+            const int sb = k & 1;
+            if (!mbar_wait(smem_addr(&state_full[sb]), (k >> 1) & 1, p.timeout_ns)) {
+                misc[kAbort] = 1;
+                if (lane == 0)
+                    report(p.status, FD_ERR_TIMEOUT);
+                break;
+            }
+            // the consumers read the next descriptor before handing item k over
+            if (misc[kAbort] || desc[((k + 1) % kDescSlots) * kDescInts + kDState] != kItemOk)
+                break;
+            const Item it = read_item(desc + (k % kDescSlots) * kDescInts);
+            finish_item<G, NC, 1, -1>(p, it, states + sb * L::kStateBytes, nullptr, misc, lane, [&] {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&state_empty[sb]));
+            });
+            if (lane == 0)
+                mbar_arrive(smem_addr(&item_empty[k % kDescSlots]));
+        }
+    }
+
+    __syncthreads();
+    if (misc[kAbort]) {
+        // Let every copy this CTA issued land before the CTA exits: the tiles
+        // (stage barriers) and each item's Q rows (descriptor barriers).
+        if (warp == kProducer && lane == 0) {
+            const int issued = misc[kIssued];
+            for (int g = max(0, issued - NS); g < issued; ++g)
+                if (!mbar_wait(smem_addr(&bars[g % NS]), (g / NS) & 1, kDrainTimeoutNs))
+                    report(p.status, FD_ERR_TIMEOUT);
+            const int descs = misc[kDescs];
+            for (int kk = max(0, descs - kDescSlots); kk < descs; ++kk)
+                if (!mbar_wait(smem_addr(&item_full[kk % kDescSlots]), (kk / kDescSlots) & 1,
+                               kDrainTimeoutNs))
+                    report(p.status, FD_ERR_TIMEOUT);
+        }
+        __syncthreads();
+        return;
+    }
+
+    // ---- the CTA's last item, closed by the whole CTA (its consumer states
+    // are in state buffer k % 2; the drained ring is the merge scratch)
+    const int k_last = misc[kFinalK];
+    finish_item<G, NC, NC + 2, 0>(p, read_item(desc + (k_last % kDescSlots) * kDescInts),
+                                  states + (k_last & 1) * L::kStateBytes, smem, misc, tid, [] {});
+    // This CTA's outputs are written: a dependent grid may launch.
+    griddep_launch_dependents();
+}
+
+// Launch shape: consumer warps, stages, resident CTAs per SM (compile-time;
+// the defaults are the measured best on GB300).
+#ifndef FD_SPLIT_CONSUMER_WARPS
+#define FD_SPLIT_CONSUMER_WARPS 4
+#endif
+#ifndef FD_SPLIT_STAGES
+#define FD_SPLIT_STAGES 4
+#endif
+#ifndef FD_SPLIT_CTAS_PER_SM
+#define FD_SPLIT_CTAS_PER_SM 2
+#endif
+constexpr int kNC = FD_SPLIT_CONSUMER_WARPS;
+constexpr int kNS = FD_SPLIT_STAGES;
+constexpr int kMinCtas = FD_SPLIT_CTAS_PER_SM;
+
+// Launch one kernel with programmatic stream serialisation, opting in to its
+// dynamic shared memory once per device (for the first 64 devices).
+template <typename Kernel>
+cudaError_t launch_kernel(Kernel kern, bool (&configured)[64], int smem_bytes, int threads,
+                          int num_ctas, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const SplitParams &p, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 64)
+            configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_ctas);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+// Stages in the ring: FP8 tiles are half the bytes, so the same 64 KB ring
+// holds twice as many (two per consumer warp).
+template <int DT>
+constexpr int stages_for()
+{
+    return DT == kKvFp8 ? 2 * kNS : kNS;
+}
+
+// One wave of items: one item per CTA.  More: the persistent kernel on
+// num_ctas CTAs.
+template <int G, int KV, int DT>
+cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitParams &p,
+                     int num_ctas, cudaStream_t stream)
+{
+    constexpr int NS = stages_for<DT>();
+    using SG = Stage<KV, DT>;
+    using LS = SingleLayout<G, kNC, NS, SG::kBytes>;
+    using LP = PersistentLayout<G, kNC, NS, SG::kBytes>;
+    static_assert(kMinCtas * (LS::kAlloc + 1024) <= 233472 && kMinCtas * (LP::kAlloc + 1024) <= 233472,
+                  "the resident CTAs must fit in shared memory");
+    if (num_ctas >= p.num_work) {
+        static bool configured[64] = {};
+        return launch_kernel(split_kv_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured, LS::kAlloc,
+                             LS::kWarps * 32, p.num_work, tk, tv, p, stream);
+    }
+    static bool configured[64] = {};
+    return launch_kernel(split_kv_persistent_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured,
+                         LP::kAlloc, LP::kWarps * 32, num_ctas, tk, tv, p, stream);
+}
+
+// Stage 1 for K/V elements of type DT: dispatch on the group size and the KV
+// layout.
+template <int DT>
+cudaError_t launch_split_dt(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
+                            int group, int num_ctas, cudaStream_t stream)
+{
+    if (num_ctas < 1 || num_ctas > p.num_work)
+        return cudaErrorInvalidValue;
+    const int kv = p.kv_last_len == nullptr ? kKvRagged
+                   : p.box_rows == kTile    ? kKvPaged
+                                            : kKvPaged16;
+    auto by_layout = [&](auto g) -> cudaError_t {
+        constexpr int G = decltype(g)::value;
+        switch (kv) {
+        case kKvRagged: return launch_g<G, kKvRagged, DT>(tm_k, tm_v, p, num_ctas, stream);
+        case kKvPaged: return launch_g<G, kKvPaged, DT>(tm_k, tm_v, p, num_ctas, stream);
+        default: return launch_g<G, kKvPaged16, DT>(tm_k, tm_v, p, num_ctas, stream);
+        }
+    };
+    switch (group) {
+    case 1: return by_layout(std::integral_constant<int, 1>{});
+    case 2: return by_layout(std::integral_constant<int, 2>{});
+    case 4: return by_layout(std::integral_constant<int, 4>{});
+    case 8: return by_layout(std::integral_constant<int, 8>{});
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+}  // namespace fd

@@ -17,7 +17,7 @@ HEADER = os.path.join(ROOT, "include", "fd.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fd_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(fd_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
 def test_exports_are_c_symbols():
     out = subprocess.run(["nm", "-D", "--defined-only", fd.lib()._name], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (fd_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (fd_[a-z0-9_]+)\b", out))
     assert set(declared_functions()) <= exported
 
 
@@ -124,7 +124,7 @@ def _prototypes():
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
     protos = {}
-    for m in re.finditer(r"\b(fd_[a-z_]+)\s*\(([^)]*)\)\s*;", text):
+    for m in re.finditer(r"\b(fd_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
         params = [p.strip() for p in m.group(2).split(",") if p.strip()]
         protos[m.group(1)] = [] if params == ["void"] else params
     return protos
