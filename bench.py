@@ -55,10 +55,11 @@ SPLIT_SOURCES = ["split_kernel.cuh", "split_kernel.cu", "split_kernel_fp8.cu", "
 
 # ----------------------------------------------------------------- helpers
 
-def step_bytes(B, Hq, Hkv, D, T, rows) -> dict:
-    """Algorithmic bytes of one step and of each kernel launch."""
+def step_bytes(B, Hq, Hkv, D, T, rows, kv_elem_bytes=2) -> dict:
+    """Algorithmic bytes of one step and of each kernel launch (K/V elements
+    of kv_elem_bytes: 2 for bf16, 1 for FP8)."""
     q = B * Hq * D * 2
-    kv = 2 * T * Hkv * D * 2
+    kv = 2 * T * Hkv * D * kv_elem_bytes
     out = B * Hq * (D + 1) * 4
     part = rows * (D + 1) * 4
     return dict(step=q + kv + out + 2 * part, split=q + kv + part, merge=part + out,
@@ -206,7 +207,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     import torch
 
     import split_kv_flashdecoding_gb300 as fd
-    from workloads import make_inputs, to_paged
+    from workloads import make_inputs, to_fp8, to_paged
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -224,8 +225,15 @@ def run_fd(args, world, rank, local) -> dict | None:
     # Steps run back to back.  K/V of one copy of the inputs must be at least
     # twice the L2 size, so no step finds the previous step's keys in L2;
     # small workloads rotate through enough copies of their inputs.
-    kv_bytes = 2 * T * Hkv * D * 2
+    fp8 = args.kv_dtype == "fp8"
+    kv_elem = 1 if fp8 else 2
+    kv_bytes = 2 * T * Hkv * D * kv_elem
     copies = max(1, -(-2 * L2_BYTES // max(kv_bytes, 1)))
+    if fp8:     # the same keys quantised to E4M3 with per-KV-head scales
+        f = to_fp8(inp)
+        inp = dict(inp, k=f["k_fp8"], v=f["v_fp8"], k_scale=f["k_scale"], v_scale=f["v_scale"])
+        k_scale_dev, v_scale_dev = f["k_scale"].to(dev), f["v_scale"].to(dev)
+        del f
     paged = args.page_size > 0
     if paged:   # the same keys in a paged KV cache (scattered pages)
         pg = to_paged(inp, args.page_size, seed=13)
@@ -244,7 +252,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     info0 = (fd.plan_paged(B, Hq, Hkv, D, args.page_size, pg_ip, pg_last) if paged
              else fd.plan(B, Hq, Hkv, D, ip_host))
     rows = info0.num_partial_rows
-    nb = step_bytes(B, Hq, Hkv, D, T, rows)
+    nb = step_bytes(B, Hq, Hkv, D, T, rows, kv_elem)
     ws_split = torch.zeros(fd.WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=dev)
     po = torch.empty((rows, D), dtype=torch.float32, device=dev)
     pl = torch.empty((rows,), dtype=torch.float32, device=dev)
@@ -261,13 +269,20 @@ def run_fd(args, world, rank, local) -> dict | None:
     # One step = fd_decode (or fd_decode_paged) through the C ABI: host plan +
     # the split kernel, which also runs stage 2 in the last CTA of each group.
     # Arguments are marshalled once so the host stays ahead of the GPU.
+    scales = (P(k_scale_dev.data_ptr()), P(v_scale_dev.data_ptr())) if fp8 else ()
     if paged:
         step_args = [(B, Hq, Hkv, D, args.page_size, num_pages, pg_ip.ctypes.data_as(P),
                       pg_last.ctypes.data_as(P), P(pg_ip_dev.data_ptr()), P(pg_last_dev.data_ptr()),
                       P(pg_idx_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()),
-                      ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()), P(ws.data_ptr()),
-                      ws.numel(), sp) for qc, kc, vc in bufs]
-        step_fn, step_name = lib.fd_decode_paged, "fd_decode_paged"
+                      *scales, ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()),
+                      P(ws.data_ptr()), ws.numel(), sp) for qc, kc, vc in bufs]
+        step_fn, step_name = ((lib.fd_decode_paged_fp8, "fd_decode_paged_fp8") if fp8
+                              else (lib.fd_decode_paged, "fd_decode_paged"))
+    elif fp8:
+        step_args = [(B, Hq, Hkv, D, ipp, P(ip_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()),
+                      P(vc.data_ptr()), *scales, ctypes.c_float(scale), P(o.data_ptr()),
+                      P(lse.data_ptr()), P(ws.data_ptr()), ws.numel(), sp) for qc, kc, vc in bufs]
+        step_fn, step_name = lib.fd_decode_fp8, "fd_decode_fp8"
     else:
         step_args = [(B, Hq, Hkv, D, ipp, P(ip_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()),
                       P(vc.data_ptr()), ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()),
@@ -314,8 +329,10 @@ def run_fd(args, world, rank, local) -> dict | None:
     ms = max_over_ranks(ev0.elapsed_time(ev1) / K, world, dev)
 
     # The dominant kernel alone (stage 1), back to back on the same stream.
-    # A paged step has no separate stage-1 entry point: its one kernel is the step.
-    if paged:
+    # A paged or FP8 step has no separate stage-1 entry point: its one kernel
+    # is the step.
+    one_kernel = paged or fp8
+    if one_kernel:
         split_avg = ms
     else:
         n_split = min(K, 500)
@@ -345,7 +362,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, fd_decode, D2H of O and LSE, all inside the events
     e2e = None
-    if not args.no_e2e and not paged:
+    if not args.no_e2e and not one_kernel:
         q_h, k_h, v_h = (inp[x].pin_memory() for x in ("q", "k", "v"))
         ip_h = inp["kv_indptr"].pin_memory()
         o_h = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
@@ -379,9 +396,13 @@ def run_fd(args, world, rank, local) -> dict | None:
     if rank != 0:
         return None
     peak, peak_kind = measured_peaks()
-    kernel_bytes = nb["step"] if paged else nb["split"]
+    kernel_bytes = nb["step"] if one_kernel else nb["split"]
+    # one item per CTA when the plan fits a wave of resident CTAs, else persistent
+    persistent = info0.num_work > info0.num_sms * info0.ctas_per_sm
+    kernel_name = ("split_kv_persistent_kernel" if persistent else "split_kv_kernel") + \
+        ("<fp8>" if fp8 else "<bf16>")
     achieved = kernel_bytes / (split_avg * 1e-3) / 1e9
-    traffic = None if paged else profiled_traffic(w.name)
+    traffic = None if one_kernel else profiled_traffic(w.name)
     gbs = aggregate_gbs(nb["step"], world, ms)
     line = {
         "metric": METRIC,
@@ -395,7 +416,8 @@ def run_fd(args, world, rank, local) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 in, fp32 accumulate/out",
+        "dtype": ("bf16 q, fp8 e4m3 K/V widened to f16, fp32 accumulate/out" if fp8
+                  else "bf16 in, fp32 accumulate/out"),
         "data": "synthetic (seeded, see workloads/)",
         "config": {"workload": w.name, "description": w.description, "batch": B,
                    "num_qo_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "total_tokens": T,
@@ -411,8 +433,10 @@ def run_fd(args, world, rank, local) -> dict | None:
                    "wall_s": round(t_wall, 3),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "kv_layout": (f"paged, page_size {args.page_size}, pages scattered in a pool"
-                                 if paged else "ragged packed")},
-        "roofline": {"bound": "hbm", "kernel": "split_kv_kernel", "achieved": round(achieved, 1),
+                                 if paged else "ragged packed"),
+                   "kv_dtype": ("fp8 e4m3, one fp32 scale per KV head for K and for V"
+                                if fp8 else "bf16")},
+        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "algorithmic_bytes_per_launch": kernel_bytes,
@@ -431,8 +455,12 @@ def run_fd(args, world, rank, local) -> dict | None:
 def _oracle_rows(inp, rows, threads) -> float:
     import oracle
     t0 = time.perf_counter()
-    oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"], rows=rows,
-                  threads=threads)
+    if "k_scale" in inp:   # FP8 K/V: the oracle dequantises, then decodes
+        oracle.decode_fp8(inp["q"], inp["k"], inp["v"], inp["k_scale"], inp["v_scale"],
+                          inp["kv_indptr"], inp["scale"], rows=rows, threads=threads)
+    else:
+        oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"], rows=rows,
+                      threads=threads)
     return time.perf_counter() - t0
 
 
@@ -513,6 +541,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[x.name for x in WORKLOADS])
     ap.add_argument("--impl", default="fd", choices=["fd", "reference"])
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="fp8: the same keys quantised to E4M3 (fd_decode_fp8)")
     ap.add_argument("--page-size", type=int, default=0,
                     help="time fd_decode_paged on the same keys laid out as a paged KV cache")
     ap.add_argument("--no-e2e", action="store_true")

@@ -51,7 +51,6 @@
 #include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -212,13 +211,17 @@ __device__ __forceinline__ float f16_round(float x)
     return __half2float(__float2half_rn(x));
 }
 
-// Two E4M3 values in the low 16 bits of x (low byte first) -> f16x2 (low
-// byte in the low half).  Every E4M3 value is an f16 value, so this is exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x)
+// Four E4M3 values (bytes 0..3 of x) -> two f16x2: lo = bytes 0, 1 and
+// hi = bytes 2, 3 (the lower byte in the lower half).  Every E4M3 value is an
+// f16 value, so this is exact.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi)
 {
-    const __half2_raw h =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
 }
 
 // Two floats -> packed bf16x2 (first argument in the low half), round to nearest.
@@ -391,8 +394,9 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int c = 4 * hc + m;
-                    mma_f16(sc[jn], qa[c][0], 0u, qa[c][1], 0u, e4m3x2_to_f16x2(kb[m]),
-                            e4m3x2_to_f16x2(kb[m] >> 16));
+                    uint32_t b0, b1;   // dims 16c + 4t4 (+1), 16c + 4t4 + 2 (+3)
+                    e4m3x4_to_f16x2x2(kb[m], b0, b1);
+                    mma_f16(sc[jn], qa[c][0], 0u, qa[c][1], 0u, b0, b1);
                 }
             }
         }
@@ -484,15 +488,14 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {         // chunk c = 2 cp + h: vb[2h] keys +0..7, vb[2h+1] +8..15
                     const int c = 2 * cp + h;
-                    // bytes of vb: key 2t4 (dim 2g, 2g+1), key 2t4+1 (dim 2g, 2g+1)
-                    const uint32_t lo_even = __byte_perm(vb[2 * h], 0u, 0x0020);
-                    const uint32_t hi_even = __byte_perm(vb[2 * h + 1], 0u, 0x0020);
-                    const uint32_t lo_odd = __byte_perm(vb[2 * h], 0u, 0x0031);
-                    const uint32_t hi_odd = __byte_perm(vb[2 * h + 1], 0u, 0x0031);
-                    mma_f16(o_acc[2 * c], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3],
-                            e4m3x2_to_f16x2(lo_even), e4m3x2_to_f16x2(hi_even));
-                    mma_f16(o_acc[2 * c + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3],
-                            e4m3x2_to_f16x2(lo_odd), e4m3x2_to_f16x2(hi_odd));
+                    // bytes of vb: key 2t4 (dim 2g, 2g+1), key 2t4+1 (dim 2g, 2g+1);
+                    // regrouped as (key 2t4, key 2t4+1) of dim 2g, then of dim 2g+1
+                    uint32_t lo_even, lo_odd, hi_even, hi_odd;
+                    e4m3x4_to_f16x2x2(__byte_perm(vb[2 * h], 0u, 0x3120), lo_even, lo_odd);
+                    e4m3x4_to_f16x2x2(__byte_perm(vb[2 * h + 1], 0u, 0x3120), hi_even, hi_odd);
+                    mma_f16(o_acc[2 * c], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], lo_even, hi_even);
+                    mma_f16(o_acc[2 * c + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], lo_odd,
+                            hi_odd);
                 }
             }
         }
