@@ -279,6 +279,36 @@ int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_
                         void *stream);
 
 /*
+ * Graph-capturable decode -- for engines that run decode steps as CUDA graphs
+ * with a fixed batch (FD++ §6 integration).  fd_decode plans on the host from
+ * the host copy of kv_indptr on every call, which a graph replay cannot
+ * repeat.  Here the plan is made once for a capacity, and each call takes
+ * device data only, so it can be captured in a CUDA graph and replayed with
+ * new lengths written to the device indptr between replays.
+ *
+ * fd_plan_graph -- host only.  Fixes the chunk length (`chunk`, or 0 for the
+ * planner's choice for max_total_tokens keys spread evenly over the batch) and
+ * sizes the plan for any kv_indptr with kv_indptr[batch] <= max_total_tokens:
+ * at most floor(max_total_tokens / chunk) + batch splits.  info->workspace_bytes
+ * is the workspace fd_decode_graph needs.
+ *
+ * fd_decode_graph -- plan + stage 1 with stage 2 fused, the split of every
+ * request derived on the device from kv_indptr_dev (same split rule as
+ * fd_plan for that chunk; an empty request gives O = 0, LSE = -inf).  Reads no
+ * host memory and makes no host-synchronising call, so it may be captured.
+ * K and V must hold at least max_total_tokens rows.  A device indptr beyond the
+ * capacity sets FD_ERR_DEVICE_BOUNDS in the status word.  Workspace as
+ * fd_decode (zero-filled once, reused across replays on one stream).
+ */
+int fd_plan_graph(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                  int64_t max_total_tokens, int num_sms, int chunk, fd_plan_info *info);
+
+int fd_decode_graph(const fd_plan_info *info, const int32_t *kv_indptr_dev,
+                    const void *q, const void *k, const void *v, float scale,
+                    float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                    void *stream);
+
+/*
  * fd_decode_static_workspace -- fd_decode for callers that cannot allocate.
  *
  * The article has no counterpart: this is a library convenience.  Some

@@ -90,6 +90,8 @@ SIGNATURES = {
     "fd_decode_paged": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P,
                          _P, _I64, _P], _I),
     "fd_decode_fp8": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
+    "fd_plan_graph": ([_I, _I, _I, _I, _I64, _I, _I, _PI], _I),
+    "fd_decode_graph": ([_PI, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
     "fd_decode_paged_fp8": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F,
                              _P, _P, _P, _I64, _P], _I),
 }
@@ -352,6 +354,26 @@ def decode_paged_fp8(q, k_pages_fp8, v_pages_fp8, k_scale, v_scale, kv_page_indp
     return o, lse
 
 
+def plan_graph(batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+               max_total_tokens: int, *, num_sms: int = 0, chunk: int = 0) -> PlanInfo:
+    """fd_plan_graph: a plan for any kv_indptr of at most max_total_tokens keys
+    (host only; fixes the chunk, sizes the workspace)."""
+    info = PlanInfo()
+    _check(lib().fd_plan_graph(batch, num_qo_heads, num_kv_heads, head_dim, int(max_total_tokens),
+                               num_sms, chunk, ctypes.byref(info)), "fd_plan_graph")
+    return info
+
+
+def decode_graph(info: PlanInfo, q, k, v, kv_indptr_dev, scale: float, o, lse, workspace,
+                 stream=None):
+    """fd_decode_graph: device data only (capturable in a CUDA graph); o, lse
+    and the workspace (info.workspace_bytes, zero-filled once) are given."""
+    _check(lib().fd_decode_graph(ctypes.byref(info), _ptr(kv_indptr_dev), _ptr(q), _ptr(k), _ptr(v),
+                                 float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "fd_decode_graph")
+
+
 def get_device_status(workspace, stream=None) -> int:
     """fd_get_device_status: synchronise, read and clear the kernels' status word."""
     return lib().fd_get_device_status(_ptr(workspace), _stream(stream))
@@ -360,7 +382,7 @@ def get_device_status(workspace, stream=None) -> int:
 __all__ = [
     "PlanInfo", "FdError", "lib", "build", "plan", "plan_work_items", "decode_split", "merge",
     "decode", "decode_static_workspace", "plan_paged", "decode_paged", "decode_fp8",
-    "decode_paged_fp8", "get_device_status",
+    "decode_paged_fp8", "plan_graph", "decode_graph", "get_device_status",
     "workspace_bytes", "num_sms",
     "status_string",
     "TILE_TOKENS", "WORKSPACE_HEADER_BYTES", "DEFAULT_TIMEOUT_NS",

@@ -268,12 +268,15 @@ __device__ __forceinline__ bool derive_split(const KeyIndex &ki, int batch, int3
 // indices that never decreases (the items of one persistent CTA).  Lane l holds
 // request b0 + l of the current window of 32 requests and the inclusive prefix
 // of the split counts; moving on to the next window costs one load per lane,
-// so a batch of at most 32 requests is read once per CTA.
+// so a batch of at most 32 requests is read once per CTA.  empty_split: an
+// empty request counts as one split of no keys (the device-side plan, where
+// that split writes the request's O = 0, LSE = -inf rows).
 struct SplitCursor {
     int32_t b0 = 0;      // first request of the window
     int32_t carry = 0;   // splits of the requests before b0
     int32_t base = 0, len = 0, pages = 0, n = 0, incl = 0;
     bool loaded = false;
+    bool empty_split = false;
 
     __device__ __forceinline__ void load(const KeyIndex &ki, int batch, int32_t chunk)
     {
@@ -282,7 +285,7 @@ struct SplitCursor {
         base = len = pages = n = 0;
         if (b < batch) {
             ki.at(b, base, len, pages);
-            n = splits_for(len, chunk);
+            n = len > 0 ? splits_for(len, chunk) : (empty_split ? 1 : 0);
         }
         incl = n;
 #pragma unroll

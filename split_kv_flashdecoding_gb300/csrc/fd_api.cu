@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <algorithm>
 #include <vector>
 
 #include "fd.h"
@@ -18,8 +19,9 @@ namespace {
 constexpr int kHeadDim = 128;
 constexpr int kBoxCols = 64;     // one 128-byte swizzle span of bf16
 // Workspace header: the status word at byte 0, the split kernel's item-claim
-// counter at byte 64 (a sector of its own).
+// counter at byte 64 and its done counter at byte 128 (sectors of their own).
 constexpr int kClaimOffset = 64;
+constexpr int kDoneOffset = 128;
 constexpr int kBoxRows = FD_TILE_TOKENS;
 
 bool aligned(const void *p, uintptr_t a)
@@ -184,7 +186,8 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
                   const int32_t *kv_indptr_dev, float scale, float *partial_o, float *partial_lse,
                   void *workspace, float *o, float *lse, int *counters,
                   const int32_t *kv_indptr_host, cudaStream_t stream,
-                  const PagedKV *paged = nullptr, const Fp8KV *fp8 = nullptr)
+                  const PagedKV *paged = nullptr, const Fp8KV *fp8 = nullptr,
+                  bool device_plan = false)
 {
     if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
         return FD_ERR_INVALID_ARG;
@@ -217,6 +220,8 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.partial_lse = partial_lse;
     p.status = static_cast<int *>(workspace);
     p.claim = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + kClaimOffset);
+    p.done = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + kDoneOffset);
+    p.device_plan = device_plan;
     p.batch = info->batch;
     p.num_qo_heads = info->num_qo_heads;
     p.num_kv_heads = info->num_kv_heads;
@@ -522,6 +527,63 @@ extern "C" int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads
                         kv_page_indptr_host, kv_last_page_len_host, kv_page_indptr_dev,
                         kv_last_page_len_dev, kv_page_indices_dev, q, k_pages_fp8, v_pages_fp8,
                         scale, o, lse, workspace, workspace_bytes, stream, &f);
+}
+
+extern "C" int fd_plan_graph(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                             int64_t max_total_tokens, int num_sms, int chunk, fd_plan_info *info)
+{
+    if (!info || batch < 0 || max_total_tokens < 0 || max_total_tokens > INT32_MAX)
+        return FD_ERR_INVALID_ARG;
+    // The chunk: the caller's, or the planner's choice for the capacity spread
+    // evenly over the batch.
+    std::vector<int32_t> even((size_t)batch + 1, 0);
+    for (int b = 1; b <= batch; ++b)
+        even[b] = (int32_t)(max_total_tokens * b / batch);
+    fd_plan_info base;
+    int rc = fd_plan(batch, num_qo_heads, num_kv_heads, head_dim, even.data(), num_sms, 0, chunk,
+                     &base);
+    if (rc != FD_OK)
+        return rc;
+    // Capacity: a request of L keys has ceil(L / C) < L / C + 1 splits and an
+    // empty one has one (it writes O = 0, LSE = -inf), so a batch of at most T
+    // keys has at most floor(T / C) + B splits.
+    const int64_t splits = max_total_tokens / base.chunk + batch;
+    if (splits * num_qo_heads > INT32_MAX)
+        return FD_ERR_INVALID_ARG;
+    *info = base;
+    info->total_splits = (int32_t)splits;
+    info->max_splits = (int32_t)std::max<int64_t>(1, (max_total_tokens + base.chunk - 1) / base.chunk);
+    info->num_work = (int32_t)(splits * num_kv_heads);
+    info->num_partial_rows = (int32_t)(splits * num_qo_heads);
+    info->total_tokens = max_total_tokens;
+    info->workspace_bytes = FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)batch * num_kv_heads * 4, 256) +
+                            round_up((int64_t)info->num_partial_rows * 4, 256) +
+                            (int64_t)info->num_partial_rows * kHeadDim * 4;
+    return FD_OK;
+}
+
+extern "C" int fd_decode_graph(const fd_plan_info *info, const int32_t *kv_indptr_dev,
+                               const void *q, const void *k, const void *v, float scale, float *o,
+                               float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    int rc = check_info(info);
+    if (rc != FD_OK)
+        return rc;
+    if (!workspace || workspace_bytes < info->workspace_bytes)
+        return FD_ERR_WORKSPACE;
+    if (info->batch == 0 || info->num_work == 0)
+        return FD_OK;
+    if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4) || !kv_indptr_dev)
+        return FD_ERR_INVALID_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int *counters = reinterpret_cast<int *>(ws + FD_WORKSPACE_HEADER_BYTES);
+    uint8_t *after =
+        ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)info->batch * info->num_kv_heads * 4, 256);
+    float *partial_lse = reinterpret_cast<float *>(after);
+    float *partial_o =
+        reinterpret_cast<float *>(after + round_up((int64_t)info->num_partial_rows * 4, 256));
+    return launch_stage1(info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace, o,
+                         lse, counters, nullptr, as_stream(stream), nullptr, nullptr, true);
 }
 
 extern "C" int fd_get_device_status(void *workspace, void *stream)

@@ -33,10 +33,15 @@ struct SplitParams {
     float *o;                   // [B, Hq, D]
     float *lse;                 // [B, Hq]
     int *counters;
-    // Persistent grid: items past the first wave are claimed from this
-    // zero-initialised counter (in the workspace header); the CTA that makes
-    // the last claim resets it.
+    // Persistent grid: items past the first wave are claimed from `claim`;
+    // every CTA adds one to `done` when it stops claiming, and the CTA that
+    // completes `done` resets both (zero-initialised, in the workspace header).
     int *claim;
+    int *done;
+    // Device-side plan (graph-capturable calls): the kernel finds the items
+    // from the device kv_indptr alone, num_work is only an upper bound, and an
+    // empty request is one split of no keys (it writes O = 0, LSE = -inf).
+    int32_t device_plan;
     int32_t indptr_in_params;   // 1: indptr_param (and last_len_param) hold the device arrays
     int32_t indptr_param[kParamIndptr];
     // Paged KV (kv_last_len non-null): K/V are page pools [num_pages, page_size,

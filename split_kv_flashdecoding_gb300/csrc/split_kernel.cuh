@@ -654,7 +654,9 @@ __device__ __forceinline__ bool item_range(const SplitParams &p, const SplitCoor
     const int32_t len = split_len_for(c.len, c.splits);
     t0 = c.s * len;
     t1 = min(t0 + len, c.len);
-    return t0 < t1 && c.base >= 0 &&
+    // under the device-side plan an empty request is one split of no keys
+    const bool empty_item = p.device_plan && c.len == 0 && c.splits == 1;
+    return (t0 < t1 || empty_item) && c.base >= 0 &&
            (PAGED ? c.base + c.pages <= p.num_page_entries : c.base + c.len <= p.total_tokens) &&
            partial_row(c.prefix, p.num_qo_heads, p.num_qo_heads - 1, c.splits, c.splits - 1) <
                p.num_partial_rows;
@@ -1066,7 +1068,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
             misc[kIssued] = 0;
             misc[kDescs] = 0;
             misc[kLast] = 0;
-            misc[kFinalK] = 0;
+            misc[kFinalK] = -1;   // set to the last item's index; stays -1 for no items
             for (int s = 0; s < NS; ++s) {
                 mbar_init(smem_addr(&bars[s]), 1);        // full: producer arrive + TMA bytes
                 mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: the stage's consumer warp
@@ -1091,6 +1093,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
         };
         const KeyIndex ki = key_index(p, paged);
         SplitCursor cursor;
+        cursor.empty_split = p.device_plan;
         TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
         int gt = 0;      // tiles issued so far (index of the stream's next tile)
         int descs = 0;   // descriptors published (lane 0)
@@ -1146,15 +1149,40 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
             return go;
         };
 
+        // Lane 0: this CTA makes no more claims.  The CTA that completes the
+        // count resets both counters for the next call; the count is
+        // acquire-release, so every CTA's claims come before the reset.
+        auto stop_claiming = [&]() {
+            cuda::atomic_ref<int, cuda::thread_scope_device> done(*p.done);
+            if (done.fetch_add(1, cuda::memory_order_acq_rel) == grid - 1) {
+                cuda::atomic_ref<int, cuda::thread_scope_device>(*p.claim).store(
+                    0, cuda::memory_order_relaxed);
+                done.store(0, cuda::memory_order_relaxed);
+            }
+        };
+
         int k = 0;
-        int32_t w = blockIdx.x;     // this item
-        int32_t nxt = p.num_work;   // the CTA's next item (lane 0; claimed during this one)
+        int32_t w = blockIdx.x;   // this item
+        int32_t nxt = 0;          // the CTA's next item (lane 0; claimed during this one)
         for (;;) {
             const int kvh = w % p.num_kv_heads;
             SplitCoord c{};
             const bool found = cursor.find(ki, p.batch, p.chunk, w / p.num_kv_heads, c);
             if (k == 0 && early_derive)
                 griddep_wait();
+            if (!found) {
+                // past the last item: the end of the CTA's stream (before its
+                // first item when the plan has fewer items than CTAs)
+                if (lane == 0) {
+                    stop_claiming();
+                    if (slot_free(k)) {
+                        desc[(k % kDescSlots) * kDescInts + kDState] = kItemEnd;
+                        ++descs;
+                        mbar_arrive(smem_addr(&item_full[k % kDescSlots]));
+                    }
+                }
+                break;
+            }
             if (lane == 0)
                 nxt = grid + atomicAdd(p.claim, 1);
             int32_t t0, t1;
@@ -1197,22 +1225,8 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
             cta_sync();
             if (!issue_range(first, n_tiles, kvh))
                 break;
-            // the next item, or the end of the CTA's stream
-            w = __shfl_sync(0xffffffffu, nxt, 0);
+            w = __shfl_sync(0xffffffffu, nxt, 0);   // the next item
             ++k;
-            if (w >= p.num_work) {
-                if (lane == 0) {
-                    // the claim that returned num_work - 1 was the grid's last one
-                    if (nxt - grid == p.num_work - 1)
-                        atomicExch(p.claim, 0);
-                    if (slot_free(k)) {
-                        desc[(k % kDescSlots) * kDescInts + kDState] = kItemEnd;
-                        ++descs;
-                        mbar_arrive(smem_addr(&item_full[k % kDescSlots]));
-                    }
-                }
-                break;
-            }
         }
         cta_sync();
         if (lane == 0) {
@@ -1301,7 +1315,15 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
         // ---------------------------------------------------------- epilogue
         // Closes every item but the CTA's last while the other warps stream on.
         __syncthreads();   // the barriers are initialised
-        for (int k = 0;; ++k) {
+        // does the CTA have an item at all?  (later items are known to exist
+        // from the descriptor checked below)
+        if (!mbar_wait(smem_addr(&item_full[0]), 0, p.timeout_ns)) {
+            misc[kAbort] = 1;
+            if (lane == 0)
+                report(p.status, FD_ERR_TIMEOUT);
+        }
+        const bool has_items = !misc[kAbort] && desc[kDState] == kItemOk;   // item 0, slot 0
+        for (int k = 0; has_items; ++k) {
             const int sb = k & 1;
             if (!mbar_wait(smem_addr(&state_full[sb]), (k >> 1) & 1, p.timeout_ns)) {
                 misc[kAbort] = 1;
@@ -1345,8 +1367,10 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
     // ---- the CTA's last item, closed by the whole CTA (its consumer states
     // are in state buffer k % 2; the drained ring is the merge scratch)
     const int k_last = misc[kFinalK];
-    finish_item<G, NC, NC + 2, 0>(p, read_item(desc + (k_last % kDescSlots) * kDescInts),
-                                  states + (k_last & 1) * L::kStateBytes, smem, misc, tid, [] {});
+    if (k_last >= 0)
+        finish_item<G, NC, NC + 2, 0>(p, read_item(desc + (k_last % kDescSlots) * kDescInts),
+                                      states + (k_last & 1) * L::kStateBytes, smem, misc, tid,
+                                      [] {});
     // This CTA's outputs are written: a dependent grid may launch.
     griddep_launch_dependents();
 }
@@ -1417,7 +1441,7 @@ cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitPa
     using LP = PersistentLayout<G, kNC, NS, SG::kBytes>;
     static_assert(kMinCtas * (LS::kAlloc + 1024) <= 233472 && kMinCtas * (LP::kAlloc + 1024) <= 233472,
                   "the resident CTAs must fit in shared memory");
-    if (num_ctas >= p.num_work) {
+    if (num_ctas >= p.num_work && !p.device_plan) {
         static bool configured[64] = {};
         return launch_kernel(split_kv_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured, LS::kAlloc,
                              LS::kWarps * 32, p.num_work, tk, tv, p, stream);
