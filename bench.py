@@ -46,6 +46,7 @@ from workloads import WORKLOADS, workload  # noqa: E402
 METRIC = "decode-attention µs/step and achieved HBM GB/s vs ~8 TB/s GB300 peak"
 DEFAULT_WORKLOAD = "gqa_b1_h32x8_l65536"
 L2_FLUSH_BYTES = 1 << 30
+GRAPH_STEPS = 8   # decode steps captured per CUDA graph with --graph
 L2_BYTES = 129 * 1000 * 1000       # GB300 L2
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
@@ -298,13 +299,44 @@ def run_fd(args, world, rank, local) -> dict | None:
         if rc != 0:
             raise fd.FdError(rc, step_name)
 
+    info_g = None
+    if args.graph:
+        # GRAPH_STEPS fd_decode_graph steps per input copy captured in one CUDA
+        # graph (device-side plan for a capacity of exactly this batch's keys),
+        # as an engine captures a decode step's many attention calls; the
+        # launches inside a graph keep their programmatic serialisation.
+        if paged or fp8:
+            raise SystemExit("--graph times the ragged bf16 path")
+        info_g = fd.plan_graph(B, Hq, Hkv, D, T)
+        ws_g = torch.zeros(info_g.workspace_bytes, dtype=torch.uint8, device=dev)
+        cap = torch.cuda.Stream(dev)
+        graphs = []
+        for qc, kc, vc in bufs:
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):   # one call outside the capture
+                fd.decode_graph(info_g, qc, kc, vc, ip_dev, scale, o, lse, ws_g, stream=cap)
+            stream.wait_stream(cap)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(GRAPH_STEPS):
+                    fd.decode_graph(info_g, qc, kc, vc, ip_dev, scale, o, lse, ws_g,
+                                    stream=torch.cuda.current_stream(dev))
+            graphs.append(g)
+        ws = ws_g
+        step_name = "fd_decode_graph"
+
+        def step(i):   # GRAPH_STEPS steps
+            graphs[i % copies].replay()
+
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
     if fd.get_device_status(ws) != 0:
         raise RuntimeError("device status set during warm-up")
 
-    K = args.steps
+    step_calls = GRAPH_STEPS if args.graph else 1   # steps per step() call
+    K = max(1, args.steps // step_calls) * step_calls
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
@@ -313,7 +345,7 @@ def run_fd(args, world, rank, local) -> dict | None:
         torch.cuda._sleep(2_000_000)        # lets the host queue steps ahead of the GPU
         t_wall0 = time.perf_counter()
         ev0.record(stream)
-        for i in range(K):
+        for i in range(K // step_calls):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
@@ -331,7 +363,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     # The dominant kernel alone (stage 1), back to back on the same stream.
     # A paged or FP8 step has no separate stage-1 entry point: its one kernel
     # is the step.
-    one_kernel = paged or fp8
+    one_kernel = paged or fp8 or args.graph
     if one_kernel:
         split_avg = ms
     else:
@@ -357,7 +389,7 @@ def run_fd(args, world, rank, local) -> dict | None:
         step(0)
         evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    flushed_ms = np.array([a.elapsed_time(b) for a, b in evs])
+    flushed_ms = np.array([a.elapsed_time(b) for a, b in evs]) / step_calls
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, fd_decode, D2H of O and LSE, all inside the events
@@ -398,7 +430,8 @@ def run_fd(args, world, rank, local) -> dict | None:
     peak, peak_kind = measured_peaks()
     kernel_bytes = nb["step"] if one_kernel else nb["split"]
     # one item per CTA when the plan fits a wave of resident CTAs, else persistent
-    persistent = info0.num_work > info0.num_sms * info0.ctas_per_sm
+    work = info_g.num_work if args.graph else info0.num_work   # the graph plan's capacity
+    persistent = work > info0.num_sms * info0.ctas_per_sm
     kernel_name = ("split_kv_persistent_kernel" if persistent else "split_kv_kernel") + \
         ("<fp8>" if fp8 else "<bf16>")
     achieved = kernel_bytes / (split_avg * 1e-3) / 1e9
@@ -435,7 +468,9 @@ def run_fd(args, world, rank, local) -> dict | None:
                    "kv_layout": (f"paged, page_size {args.page_size}, pages scattered in a pool"
                                  if paged else "ragged packed"),
                    "kv_dtype": ("fp8 e4m3, one fp32 scale per KV head for K and for V"
-                                if fp8 else "bf16")},
+                                if fp8 else "bf16"),
+                   "launch": ("CUDA graph replay of fd_decode_graph (device-side plan)"
+                              if args.graph else "C ABI call per step (host plan)")},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
@@ -541,6 +576,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[x.name for x in WORKLOADS])
     ap.add_argument("--impl", default="fd", choices=["fd", "reference"])
+    ap.add_argument("--graph", action="store_true",
+                    help="time CUDA-graph replays of fd_decode_graph (device-side plan)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="fp8: the same keys quantised to E4M3 (fd_decode_fp8)")
     ap.add_argument("--page-size", type=int, default=0,

@@ -224,9 +224,11 @@ struct SplitCoord {
 
 // Warp-collective: locate global split `j` (if by_request is false) or request
 // `j` (if true) by scanning the requests' key counts.  All lanes return the
-// same result; returns false if j is out of range.
+// same result; returns false if j is out of range.  empty_split: an empty
+// request counts as one split (the device-side plan).
 __device__ __forceinline__ bool derive_split(const KeyIndex &ki, int batch, int32_t chunk, int32_t j,
-                                             bool by_request, SplitCoord &out)
+                                             bool by_request, SplitCoord &out,
+                                             bool empty_split = false)
 {
     const int lane = threadIdx.x & 31;
     int32_t carry = 0;
@@ -235,7 +237,7 @@ __device__ __forceinline__ bool derive_split(const KeyIndex &ki, int batch, int3
         int32_t base = 0, len = 0, pages = 0, n = 0;
         if (b < batch) {
             ki.at(b, base, len, pages);
-            n = len > 0 ? splits_for(len, chunk) : 0;
+            n = len > 0 ? splits_for(len, chunk) : (empty_split ? 1 : 0);
         }
         int32_t incl = n;
 #pragma unroll

@@ -905,14 +905,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         // barrier operations and the copies.
         SplitCoord c{};
         const bool found = derive_split(key_index(p, paged), p.batch, p.chunk,
-                                        blockIdx.x / p.num_kv_heads, false, c);
+                                        blockIdx.x / p.num_kv_heads, false, c, p.device_plan);
         if (early_derive)
             griddep_wait();
         int32_t t0, t1;
         const bool ok = item_range<paged>(p, c, found, t0, t1);
+        // the device-side plan launches a CTA per item of its capacity; those
+        // past the batch's items have nothing to do
+        const bool none = !found && p.device_plan;
         if (lane == 0) {
-            write_desc(desc, c, t0, t1, kvh, 0, ok ? kItemOk : kItemBad);
-            misc[kAbort] = ok ? 0 : 1;
+            write_desc(desc, c, t0, t1, kvh, 0, ok ? kItemOk : (none ? kItemEnd : kItemBad));
+            misc[kAbort] = ok || none ? 0 : 1;
             misc[kIssued] = 0;
             misc[kLast] = 0;
             for (int s = 0; s < NS; ++s) {
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                 mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: the stage's consumer warp
             }
             fence_mbar_init();
-            if (!ok)
+            if (!ok && !none)
                 report(p.status, FD_ERR_DEVICE_BOUNDS);
         }
         __syncwarp();
@@ -1011,6 +1014,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     }
     // ---- close the item: consumer states over the drained ring, then the
     // whole CTA combines them (and runs stage 2 as the group's last CTA)
+    if (read_item(desc).state != kItemOk) {   // a CTA without an item (device-side plan)
+        griddep_launch_dependents();
+        return;
+    }
     if (warp < NC)
         write_state<G, NC, DT>(smem, warp, lane, o_acc, m_run, l_part, vscale);
     __syncthreads();
@@ -1441,7 +1448,7 @@ cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitPa
     using LP = PersistentLayout<G, kNC, NS, SG::kBytes>;
     static_assert(kMinCtas * (LS::kAlloc + 1024) <= 233472 && kMinCtas * (LP::kAlloc + 1024) <= 233472,
                   "the resident CTAs must fit in shared memory");
-    if (num_ctas >= p.num_work && !p.device_plan) {
+    if (num_ctas >= p.num_work) {   // one wave: one item (or, device-side plan, at most one) per CTA
         static bool configured[64] = {};
         return launch_kernel(split_kv_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured, LS::kAlloc,
                              LS::kWarps * 32, p.num_work, tk, tv, p, stream);

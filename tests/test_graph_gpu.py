@@ -101,3 +101,42 @@ def test_indptr_beyond_capacity_is_flagged(cuda_device):
     fd.decode_graph(info, q, k, v, ip, 0.1, o, lse, ws)
     torch.cuda.synchronize()
     assert fd.get_device_status(ws) == -6
+
+
+@pytest.mark.parametrize("lengths", [[1000, 0, 1999], [0, 0, 0], [3000, 0, 0], [1, 1, 1]])
+def test_device_plan_in_one_wave(cuda_device, lengths):
+    """A capacity whose plan fits one wave of CTAs runs the one-item-per-CTA
+    kernel under the device-side plan (CTAs past the batch's items exit), also
+    captured in a CUDA graph."""
+    b, cap = 3, 3000
+    info = fd.plan_graph(b, 16, 8, D, cap)
+    assert info.num_work <= info.num_sms * info.ctas_per_sm, "the plan must fit one wave"
+    dev = cuda_device
+    inp = make_small(b, 16, 8, D, lengths, seed=sum(lengths) % 997)
+    T = int(inp["kv_indptr"][-1])
+    q = inp["q"].to(dev)
+    k = torch.zeros((cap, 8, D), dtype=torch.bfloat16, device=dev)
+    v = torch.zeros_like(k)
+    k[:T].copy_(inp["k"])
+    v[:T].copy_(inp["v"])
+    ip = inp["kv_indptr"].to(dev)
+    o = torch.empty((b, 16, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((b, 16), dtype=torch.float32, device=dev)
+    ws = torch.zeros(info.workspace_bytes, dtype=torch.uint8, device=dev)
+    o_ref, lse_ref = oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"])
+    fd.decode_graph(info, q, k, v, ip, inp["scale"], o, lse, ws)
+    torch.cuda.synchronize()
+    assert fd.get_device_status(ws) == 0
+    err = errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
+    assert_within(err, **TIGHT, what=f"{lengths}")
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    o.fill_(7.0)
+    with torch.cuda.graph(g, stream=s):
+        fd.decode_graph(info, q, k, v, ip, inp["scale"], o, lse, ws,
+                        stream=torch.cuda.current_stream(dev))
+    g.replay()
+    torch.cuda.synchronize()
+    err = errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
+    assert_within(err, **TIGHT, what=f"{lengths} (graph)")
