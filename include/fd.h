@@ -309,6 +309,22 @@ int fd_decode_graph(const fd_plan_info *info, const int32_t *kv_indptr_dev,
                     void *stream);
 
 /*
+ * fd_merge_states -- the merge of attention states computed over disjoint
+ * parts of the same keys: the exchange step of sequence sharding (one
+ * request's keys cut into contiguous shards on several GPUs, each running
+ * fd_decode on its shard; the per-shard O and LSE are gathered and merged
+ * here).  FD++ §3 stage 2: the same global reduction, now across shards.
+ *
+ * For each row r: M = max_s lse_states[s][r], w_s = exp(lse_states[s][r] - M),
+ * o[r] = sum_s w_s o_states[s][r] / sum_s w_s, lse[r] = M + ln sum_s w_s; a
+ * row whose states are all -inf (no keys in any shard) gets o = 0, lse = -inf.
+ * o_states fp32 [num_states, rows, head_dim], lse_states fp32 [num_states,
+ * rows], o [rows, head_dim], lse [rows], all on the device; rows = B * Hq.
+ */
+int fd_merge_states(int num_states, int rows, int head_dim, const float *o_states,
+                    const float *lse_states, float *o, float *lse, void *stream);
+
+/*
  * fd_decode_static_workspace -- fd_decode for callers that cannot allocate.
  *
  * The article has no counterpart: this is a library convenience.  Some

@@ -91,6 +91,7 @@ SIGNATURES = {
                          _P, _I64, _P], _I),
     "fd_decode_fp8": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
     "fd_plan_graph": ([_I, _I, _I, _I, _I64, _I, _I, _PI], _I),
+    "fd_merge_states": ([_I, _I, _I, _P, _P, _P, _P, _P], _I),
     "fd_decode_graph": ([_PI, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
     "fd_decode_paged_fp8": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F,
                              _P, _P, _P, _I64, _P], _I),
@@ -374,6 +375,21 @@ def decode_graph(info: PlanInfo, q, k, v, kv_indptr_dev, scale: float, o, lse, w
            "fd_decode_graph")
 
 
+def merge_states(o_states, lse_states, *, o=None, lse=None, stream=None):
+    """fd_merge_states: o_states fp32 [S, ..., D] and lse_states fp32 [S, ...]
+    (S attention states over disjoint parts of the keys) -> merged (O, LSE)."""
+    import torch
+    S, D = o_states.shape[0], o_states.shape[-1]
+    rows = lse_states[0].numel()
+    if o is None:
+        o = torch.empty(o_states.shape[1:], dtype=torch.float32, device=o_states.device)
+    if lse is None:
+        lse = torch.empty(lse_states.shape[1:], dtype=torch.float32, device=lse_states.device)
+    _check(lib().fd_merge_states(S, rows, D, _ptr(o_states), _ptr(lse_states), _ptr(o), _ptr(lse),
+                                 _stream(stream)), "fd_merge_states")
+    return o, lse
+
+
 def get_device_status(workspace, stream=None) -> int:
     """fd_get_device_status: synchronise, read and clear the kernels' status word."""
     return lib().fd_get_device_status(_ptr(workspace), _stream(stream))
@@ -382,7 +398,7 @@ def get_device_status(workspace, stream=None) -> int:
 __all__ = [
     "PlanInfo", "FdError", "lib", "build", "plan", "plan_work_items", "decode_split", "merge",
     "decode", "decode_static_workspace", "plan_paged", "decode_paged", "decode_fp8",
-    "decode_paged_fp8", "plan_graph", "decode_graph", "get_device_status",
+    "decode_paged_fp8", "plan_graph", "decode_graph", "merge_states", "get_device_status",
     "workspace_bytes", "num_sms",
     "status_string",
     "TILE_TOKENS", "WORKSPACE_HEADER_BYTES", "DEFAULT_TIMEOUT_NS",

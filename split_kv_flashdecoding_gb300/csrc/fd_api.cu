@@ -586,6 +586,23 @@ extern "C" int fd_decode_graph(const fd_plan_info *info, const int32_t *kv_indpt
                          lse, counters, nullptr, as_stream(stream), nullptr, nullptr, true);
 }
 
+extern "C" int fd_merge_states(int num_states, int rows, int head_dim, const float *o_states,
+                               const float *lse_states, float *o, float *lse, void *stream)
+{
+    if (head_dim != kHeadDim)
+        return FD_ERR_UNSUPPORTED;
+    if (num_states < 1 || rows < 0 || (int64_t)num_states * rows > INT32_MAX)
+        return FD_ERR_INVALID_ARG;
+    if (rows == 0)
+        return FD_OK;
+    if (!o_states || !lse_states || !o || !lse || !aligned(o_states, 16) || !aligned(o, 16) ||
+        !aligned(lse_states, 4) || !aligned(lse, 4))
+        return FD_ERR_INVALID_ARG;
+    const cudaError_t e =
+        fd::launch_merge_states(num_states, rows, o_states, lse_states, o, lse, as_stream(stream));
+    return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
 extern "C" int fd_get_device_status(void *workspace, void *stream)
 {
     if (!workspace)

@@ -94,4 +94,9 @@ int split_ctas_per_sm();
 // dependent of the preceding grid so its launch overlaps that grid's tail.
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 
+// Merge of num_states attention states per row (o_states [num_states][rows][D],
+// lse_states [num_states][rows]) into o [rows][D], lse [rows].
+cudaError_t launch_merge_states(int num_states, int rows, const float *o_states,
+                                const float *lse_states, float *o, float *lse, cudaStream_t stream);
+
 }  // namespace fd

@@ -142,6 +142,69 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 
 }  // namespace
 
+namespace {
+
+// Merge of R attention states per row (the sequence-sharded exchange): for
+// row r, M = max_s LSE_s, w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s,
+// LSE = M + ln sum_s w_s; a row whose states are all empty (LSE = -inf) gets
+// O = 0, LSE = -inf.  One warp per row, lane = 4 columns (one float4).
+constexpr int kStatesWarps = 4;
+
+__global__ void __launch_bounds__(kStatesWarps * 32)
+    merge_states_kernel(int num_states, int rows, const float *__restrict__ o_states,
+                        const float *__restrict__ lse_states, float *__restrict__ o,
+                        float *__restrict__ lse)
+{
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kStatesWarps + (threadIdx.x >> 5);
+    if (row < rows) {
+        float m = -INFINITY;
+        for (int s = 0; s < num_states; ++s)
+            m = fmaxf(m, __ldg(lse_states + (int64_t)s * rows + row));
+        float den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m != -INFINITY) {
+            for (int s = 0; s < num_states; ++s) {
+                const int64_t r = (int64_t)s * rows + row;
+                const float w = expf(__ldg(lse_states + r) - m);
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(o_states + r * kHeadDim) + lane);
+                den += w;
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        reinterpret_cast<float4 *>(o + (int64_t)row * kHeadDim)[lane] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (lane == 0)
+            lse[row] = den > 0.f ? m + logf(den) : -INFINITY;
+    }
+    griddep_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_merge_states(int num_states, int rows, const float *o_states,
+                                const float *lse_states, float *o, float *lse, cudaStream_t stream)
+{
+    if (rows == 0)
+        return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + kStatesWarps - 1) / kStatesWarps));
+    cfg.blockDim = dim3(kStatesWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_states_kernel, num_states, rows, o_states, lse_states, o, lse);
+}
+
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream)
 {
     const int64_t ctas = (int64_t)p.batch * p.num_qo_heads;
