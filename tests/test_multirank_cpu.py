@@ -48,7 +48,7 @@ def _rank_main(rank, world, port, out):
 def test_two_gloo_ranks_time_and_shard():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
