@@ -50,17 +50,24 @@ GRAPH_STEPS = 8   # decode steps captured per CUDA graph with --graph
 L2_BYTES = 129 * 1000 * 1000       # GB300 L2
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-SPLIT_SOURCES = ["split_kernel.cuh", "split_kernel.cu", "split_kernel_fp8.cu", "device_common.cuh",
-                 "plan_rule.h", "fd_api.cu"]
+SPLIT_SOURCES = ["split_kernel.cuh", "split_kernel.cu", "split_kernel_fp8.cu", "split_kernel_int4.cu",
+                 "device_common.cuh", "plan_rule.h", "fd_api.cu"]
 
 
 # ----------------------------------------------------------------- helpers
 
-def step_bytes(B, Hq, Hkv, D, T, rows, kv_elem_bytes=2) -> dict:
-    """Algorithmic bytes of one step and of each kernel launch (K/V elements
-    of kv_elem_bytes: 2 for bf16, 1 for FP8)."""
+def kv_row_bytes(kv_dtype: str, D: int) -> int:
+    """Bytes of one key row of one KV head in K (or V): bf16 2 per element,
+    FP8 1 (its per-head scale is a few bytes per step), INT4 half a byte plus
+    the row's fp32 scale."""
+    return {"bf16": 2 * D, "fp8": D, "int4": D // 2 + 4}[kv_dtype]
+
+
+def step_bytes(B, Hq, Hkv, D, T, rows, row_bytes=None) -> dict:
+    """Algorithmic bytes of one step and of each kernel launch (K and V rows
+    of row_bytes each per KV head; bf16 by default)."""
     q = B * Hq * D * 2
-    kv = 2 * T * Hkv * D * kv_elem_bytes
+    kv = 2 * T * Hkv * (2 * D if row_bytes is None else row_bytes)
     out = B * Hq * (D + 1) * 4
     part = rows * (D + 1) * 4
     return dict(step=q + kv + out + 2 * part, split=q + kv + part, merge=part + out,
@@ -208,7 +215,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     import torch
 
     import split_kv_flashdecoding_gb300 as fd
-    from workloads import make_inputs, to_fp8, to_paged
+    from workloads import make_inputs, to_fp8, to_int4, to_paged, to_paged_int4
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -227,15 +234,28 @@ def run_fd(args, world, rank, local) -> dict | None:
     # twice the L2 size, so no step finds the previous step's keys in L2;
     # small workloads rotate through enough copies of their inputs.
     fp8 = args.kv_dtype == "fp8"
-    kv_elem = 1 if fp8 else 2
-    kv_bytes = 2 * T * Hkv * D * kv_elem
+    int4 = args.kv_dtype == "int4"
+    quant = fp8 or int4
+    row_bytes = kv_row_bytes(args.kv_dtype, D)
+    kv_bytes = 2 * T * Hkv * row_bytes
     copies = max(1, -(-2 * L2_BYTES // max(kv_bytes, 1)))
+    paged = args.page_size > 0
     if fp8:     # the same keys quantised to E4M3 with per-KV-head scales
         f = to_fp8(inp)
         inp = dict(inp, k=f["k_fp8"], v=f["v_fp8"], k_scale=f["k_scale"], v_scale=f["v_scale"])
         k_scale_dev, v_scale_dev = f["k_scale"].to(dev), f["v_scale"].to(dev)
         del f
-    paged = args.page_size > 0
+    if int4:    # the same keys quantised to INT4 with one scale per key row and KV head
+        f = to_int4(inp)
+        if paged:
+            pgi = to_paged_int4(f, args.page_size, seed=13)
+            k_scale_dev, v_scale_dev = pgi["k_scale_pages"].to(dev), pgi["v_scale_pages"].to(dev)
+            del pgi
+        else:
+            k_scale_dev, v_scale_dev = f["k_scale_int4"].to(dev), f["v_scale_int4"].to(dev)
+        inp = dict(inp, k=f["k_int4"], v=f["v_int4"], k_scale=f["k_scale_int4"],
+                   v_scale=f["v_scale_int4"], int4=True)
+        del f
     if paged:   # the same keys in a paged KV cache (scattered pages)
         pg = to_paged(inp, args.page_size, seed=13)
         bufs = [tuple(pg[x].to(dev) for x in ("q", "k_pages", "v_pages")) for _ in range(copies)]
@@ -253,7 +273,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     info0 = (fd.plan_paged(B, Hq, Hkv, D, args.page_size, pg_ip, pg_last) if paged
              else fd.plan(B, Hq, Hkv, D, ip_host))
     rows = info0.num_partial_rows
-    nb = step_bytes(B, Hq, Hkv, D, T, rows, kv_elem)
+    nb = step_bytes(B, Hq, Hkv, D, T, rows, row_bytes)
     ws_split = torch.zeros(fd.WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=dev)
     po = torch.empty((rows, D), dtype=torch.float32, device=dev)
     pl = torch.empty((rows,), dtype=torch.float32, device=dev)
@@ -270,20 +290,22 @@ def run_fd(args, world, rank, local) -> dict | None:
     # One step = fd_decode (or fd_decode_paged) through the C ABI: host plan +
     # the split kernel, which also runs stage 2 in the last CTA of each group.
     # Arguments are marshalled once so the host stays ahead of the GPU.
-    scales = (P(k_scale_dev.data_ptr()), P(v_scale_dev.data_ptr())) if fp8 else ()
+    scales = (P(k_scale_dev.data_ptr()), P(v_scale_dev.data_ptr())) if quant else ()
     if paged:
         step_args = [(B, Hq, Hkv, D, args.page_size, num_pages, pg_ip.ctypes.data_as(P),
                       pg_last.ctypes.data_as(P), P(pg_ip_dev.data_ptr()), P(pg_last_dev.data_ptr()),
                       P(pg_idx_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()),
                       *scales, ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()),
                       P(ws.data_ptr()), ws.numel(), sp) for qc, kc, vc in bufs]
-        step_fn, step_name = ((lib.fd_decode_paged_fp8, "fd_decode_paged_fp8") if fp8
-                              else (lib.fd_decode_paged, "fd_decode_paged"))
-    elif fp8:
+        step_name = ("fd_decode_paged_fp8" if fp8 else "fd_decode_paged_int4" if int4
+                     else "fd_decode_paged")
+        step_fn = getattr(lib, step_name)
+    elif quant:
         step_args = [(B, Hq, Hkv, D, ipp, P(ip_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()),
                       P(vc.data_ptr()), *scales, ctypes.c_float(scale), P(o.data_ptr()),
                       P(lse.data_ptr()), P(ws.data_ptr()), ws.numel(), sp) for qc, kc, vc in bufs]
-        step_fn, step_name = lib.fd_decode_fp8, "fd_decode_fp8"
+        step_name = "fd_decode_fp8" if fp8 else "fd_decode_int4"
+        step_fn = getattr(lib, step_name)
     else:
         step_args = [(B, Hq, Hkv, D, ipp, P(ip_dev.data_ptr()), P(qc.data_ptr()), P(kc.data_ptr()),
                       P(vc.data_ptr()), ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()),
@@ -305,7 +327,7 @@ def run_fd(args, world, rank, local) -> dict | None:
         # graph (device-side plan for a capacity of exactly this batch's keys),
         # as an engine captures a decode step's many attention calls; the
         # launches inside a graph keep their programmatic serialisation.
-        if paged or fp8:
+        if paged or quant:
             raise SystemExit("--graph times the ragged bf16 path")
         info_g = fd.plan_graph(B, Hq, Hkv, D, T)
         ws_g = torch.zeros(info_g.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -361,9 +383,9 @@ def run_fd(args, world, rank, local) -> dict | None:
     ms = max_over_ranks(ev0.elapsed_time(ev1) / K, world, dev)
 
     # The dominant kernel alone (stage 1), back to back on the same stream.
-    # A paged or FP8 step has no separate stage-1 entry point: its one kernel
-    # is the step.
-    one_kernel = paged or fp8 or args.graph
+    # A paged, FP8 or INT4 step has no separate stage-1 entry point: its one
+    # kernel is the step.
+    one_kernel = paged or quant or args.graph
     if one_kernel:
         split_avg = ms
     else:
@@ -433,7 +455,7 @@ def run_fd(args, world, rank, local) -> dict | None:
     work = info_g.num_work if args.graph else info0.num_work   # the graph plan's capacity
     persistent = work > info0.num_sms * info0.ctas_per_sm
     kernel_name = ("split_kv_persistent_kernel" if persistent else "split_kv_kernel") + \
-        ("<fp8>" if fp8 else "<bf16>")
+        ("<fp8>" if fp8 else "<int4>" if int4 else "<bf16>")
     achieved = kernel_bytes / (split_avg * 1e-3) / 1e9
     traffic = None if one_kernel else profiled_traffic(w.name)
     gbs = aggregate_gbs(nb["step"], world, ms)
@@ -450,6 +472,7 @@ def run_fd(args, world, rank, local) -> dict | None:
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": ("bf16 q, fp8 e4m3 K/V widened to f16, fp32 accumulate/out" if fp8
+                  else "bf16 q, int4 K/V widened to bf16, fp32 scales/accumulate/out" if int4
                   else "bf16 in, fp32 accumulate/out"),
         "data": "synthetic (seeded, see workloads/)",
         "config": {"workload": w.name, "description": w.description, "batch": B,
@@ -468,7 +491,9 @@ def run_fd(args, world, rank, local) -> dict | None:
                    "kv_layout": (f"paged, page_size {args.page_size}, pages scattered in a pool"
                                  if paged else "ragged packed"),
                    "kv_dtype": ("fp8 e4m3, one fp32 scale per KV head for K and for V"
-                                if fp8 else "bf16"),
+                                if fp8 else
+                                "int4 (two's complement, 2 per byte), one fp32 scale per key row "
+                                "and KV head for K and for V" if int4 else "bf16"),
                    "launch": ("CUDA graph replay of fd_decode_graph (device-side plan)"
                               if args.graph else "C ABI call per step (host plan)")},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
@@ -490,7 +515,10 @@ def run_fd(args, world, rank, local) -> dict | None:
 def _oracle_rows(inp, rows, threads) -> float:
     import oracle
     t0 = time.perf_counter()
-    if "k_scale" in inp:   # FP8 K/V: the oracle dequantises, then decodes
+    if inp.get("int4"):    # INT4 K/V: the oracle dequantises, then decodes
+        oracle.decode_int4(inp["q"], inp["k"], inp["v"], inp["k_scale"], inp["v_scale"],
+                           inp["kv_indptr"], inp["scale"], rows=rows, threads=threads)
+    elif "k_scale" in inp:   # FP8 K/V: the oracle dequantises, then decodes
         oracle.decode_fp8(inp["q"], inp["k"], inp["v"], inp["k_scale"], inp["v_scale"],
                           inp["kv_indptr"], inp["scale"], rows=rows, threads=threads)
     else:
@@ -578,8 +606,9 @@ def main():
     ap.add_argument("--impl", default="fd", choices=["fd", "reference"])
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of fd_decode_graph (device-side plan)")
-    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
-                    help="fp8: the same keys quantised to E4M3 (fd_decode_fp8)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8", "int4"], default="bf16",
+                    help="fp8: the same keys quantised to E4M3 (fd_decode_fp8); int4: to packed "
+                         "four-bit codes with per-row scales (fd_decode_int4)")
     ap.add_argument("--page-size", type=int, default=0,
                     help="time fd_decode_paged on the same keys laid out as a paged KV cache")
     ap.add_argument("--no-e2e", action="store_true")

@@ -279,6 +279,44 @@ int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_
                         void *stream);
 
 /*
+ * INT4 KV cache -- FD++ §4 names INT4 beside FP8: the packed codes are read
+ * from HBM as they are and widened on chip, in registers, into the
+ * tensor-core operands, so the stream moves about a quarter of the bytes of
+ * bf16.  The page fixes no INT4 format; this is the plainest one that keeps a
+ * head's values on a common scale per key: symmetric codes, one scale per
+ * (key row, KV head).
+ *
+ * Layout: K and V hold head_dim / 2 bytes per (row, KV head): [T, Hkv, D/2]
+ * ragged, [num_pages, page_size, Hkv, D/2] paged.  Byte j of a row holds
+ * element 2j in its low nibble and element 2j + 1 in its high nibble, each a
+ * four-bit two's-complement code c in -8..7.  k_scale and v_scale (device,
+ * fp32, 16-byte aligned) are head-major: [Hkv][rows], rows = T (ragged) or
+ * num_pages * page_size (paged; entry h * rows + p * page_size + r belongs to
+ * row r of page p).  The value of a K element is c * k_scale[h][row], and
+ * likewise for V.  q stays bf16 and O, LSE fp32; the result is attention over
+ * the dequantised K and V (the codes widen to bf16 exactly; each row's K scale
+ * multiplies its logit and its V scale its softmax weight in P V, all in
+ * fp32).  A scale of +-inf or NaN propagates.  Num_kv_heads * rows must stay
+ * below 2^31 - 64, else FD_ERR_UNSUPPORTED.  Workspace and plan as for
+ * fd_decode / fd_decode_paged.
+ */
+int fd_decode_int4(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                   const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+                   const void *q, const void *k_int4, const void *v_int4,
+                   const float *k_scale, const float *v_scale, float scale,
+                   float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                   void *stream);
+
+int fd_decode_paged_int4(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                         int page_size, int num_pages, const int32_t *kv_page_indptr_host,
+                         const int32_t *kv_last_page_len_host, const int32_t *kv_page_indptr_dev,
+                         const int32_t *kv_last_page_len_dev, const int32_t *kv_page_indices_dev,
+                         const void *q, const void *k_pages_int4, const void *v_pages_int4,
+                         const float *k_scale, const float *v_scale, float scale,
+                         float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                         void *stream);
+
+/*
  * Graph-capturable decode -- for engines that run decode steps as CUDA graphs
  * with a fixed batch (FD++ §6 integration).  fd_decode plans on the host from
  * the host copy of kv_indptr on every call, which a graph replay cannot

@@ -19,6 +19,11 @@ two-stage global reduction".
   dequant_fp8(codes, s)   K or V codes [T, Hkv, D] times a per-KV-head scale
   decode_fp8(...)         decode() on exactly dequantised FP8 K/V (§4: the
                           quantised cache is dequantised, then attended over)
+  int4_codes(packed)      packed four-bit two's-complement codes -> integers
+                          (§4 names INT4 K/V beside FP8)
+  dequant_int4(codes, s)  K or V codes [rows, Hkv, D/2] times a per-(row, KV
+                          head) scale [Hkv, rows]
+  decode_int4(...)        decode() on exactly dequantised INT4 K/V
 
 The arithmetic is in fd_oracle.c (fp64 throughout); this module only
 marshals arrays.  build() compiles it with gcc.
@@ -266,4 +271,45 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, kv_indptr, scale, rows=Non
     """decode() on FP8 K/V: both are dequantised exactly (dequant_fp8) and q
     is widened to fp64, then the same unsplit definition runs in fp64."""
     return decode(_bf16_to_f64(q), dequant_fp8(k_codes, k_scale), dequant_fp8(v_codes, v_scale),
+                  kv_indptr, scale, rows=rows, threads=threads)
+
+
+def int4_codes(packed) -> np.ndarray:
+    """Packed four-bit two's-complement codes -> int64 values, two per byte.
+
+    Byte j of a row holds element 2j in its low nibble and element 2j + 1 in
+    its high nibble; a nibble n stands for n - 16 when n >= 8 (so -8..7).
+    packed [..., D/2] uint8 -> [..., D].
+    """
+    try:
+        import torch
+        if isinstance(packed, torch.Tensor):
+            packed = packed.detach().cpu().contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    b = np.asarray(packed).astype(np.int64)
+    nib = np.stack([b & 0xF, (b >> 4) & 0xF], axis=-1).reshape(*b.shape[:-1], 2 * b.shape[-1])
+    return np.where(nib >= 8, nib - 16, nib)
+
+
+def dequant_int4(packed, scale) -> np.ndarray:
+    """K or V as packed INT4 codes [rows, Hkv, D/2] with one fp32 scale per
+    (row, KV head), stored head-major [Hkv, rows] -> fp64 values
+    code * scale[h, row] [rows, Hkv, D] (exact: 4-bit codes times 24 bits)."""
+    try:
+        import torch
+        if isinstance(scale, torch.Tensor):
+            scale = scale.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    vals = int4_codes(packed).astype(np.float64)
+    s = np.asarray(scale, dtype=np.float32).astype(np.float64)   # [Hkv, rows]
+    return vals * s.T[:, :, None]
+
+
+def decode_int4(q, k_packed, v_packed, k_scale, v_scale, kv_indptr, scale, rows=None,
+                threads: int | None = None):
+    """decode() on INT4 K/V: both are dequantised exactly (dequant_int4) and q
+    is widened to fp64, then the same unsplit definition runs in fp64."""
+    return decode(_bf16_to_f64(q), dequant_int4(k_packed, k_scale), dequant_int4(v_packed, v_scale),
                   kv_indptr, scale, rows=rows, threads=threads)

@@ -13,6 +13,10 @@ Entry points (same names as the C ABI, minus the ``fd_`` prefix):
   decode_static_workspace(...)          the same for callers that cannot allocate
                                         (scratch in a fixed array in the library)
   plan_paged(...), decode_paged(...)    the same over a paged KV cache (page tables)
+  decode_fp8(...), decode_paged_fp8()   FP8 (E4M3) K/V, one scale per KV head
+  decode_int4(...), decode_paged_int4() INT4 K/V, one scale per key row and KV head
+  plan_graph(...), decode_graph(...)    graph-capturable decode (device-side plan)
+  merge_states(...)                     merge attention states (sequence shards)
   get_device_status(workspace)          read and clear the kernels' error word
 
 There is no CPU fallback: if libfd.so cannot be loaded, importing the library
@@ -95,6 +99,9 @@ SIGNATURES = {
     "fd_decode_graph": ([_PI, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
     "fd_decode_paged_fp8": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F,
                              _P, _P, _P, _I64, _P], _I),
+    "fd_decode_int4": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _I64, _P], _I),
+    "fd_decode_paged_int4": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F,
+                              _P, _P, _P, _I64, _P], _I),
 }
 
 
@@ -355,6 +362,68 @@ def decode_paged_fp8(q, k_pages_fp8, v_pages_fp8, k_scale, v_scale, kv_page_indp
     return o, lse
 
 
+def _int4_bytes(x, D: int):
+    """Packed INT4 K/V: uint8 with D / 2 bytes per (row, KV head)."""
+    import torch
+    if x.dtype != torch.uint8 or x.shape[-1] != D // 2:
+        raise FdError(-1, "INT4 K/V must be uint8 [..., Hkv, head_dim / 2]")
+    return x
+
+
+def decode_int4(q, k_int4, v_int4, k_scale, v_scale, kv_indptr_host, kv_indptr_dev, scale: float, *,
+                o=None, lse=None, workspace=None, stream=None):
+    """fd_decode_int4: q [B,Hq,D] bf16, k/v [T,Hkv,D/2] packed four-bit codes
+    (uint8), k_scale / v_scale fp32 [Hkv, T] CUDA tensors -> (O, LSE) fp32."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv = k_int4.shape[1]
+    ip = _host_indptr(kv_indptr_host)
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = plan(B, Hq, Hkv, D, ip).workspace_bytes
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    _check(lib().fd_decode_int4(B, Hq, Hkv, D, ip.ctypes.data_as(ctypes.c_void_p),
+                                _ptr(kv_indptr_dev), _ptr(q), _ptr(_int4_bytes(k_int4, D)),
+                                _ptr(_int4_bytes(v_int4, D)), _ptr(k_scale), _ptr(v_scale),
+                                float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "fd_decode_int4")
+    return o, lse
+
+
+def decode_paged_int4(q, k_pages_int4, v_pages_int4, k_scale, v_scale, kv_page_indptr_host,
+                      kv_last_page_len_host, kv_page_indptr_dev, kv_last_page_len_dev,
+                      kv_page_indices_dev, scale: float, *, o=None, lse=None, workspace=None,
+                      stream=None):
+    """fd_decode_paged_int4: fd_decode_paged over packed INT4 page pools
+    [num_pages, page_size, Hkv, D/2] with fp32 scales [Hkv, num_pages * page_size]."""
+    import torch
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv = k_pages_int4.shape[0], k_pages_int4.shape[1], k_pages_int4.shape[2]
+    ip = _host_indptr(kv_page_indptr_host)
+    ll = _host_indptr(kv_last_page_len_host)
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = plan_paged(B, Hq, Hkv, D, page_size, ip, ll).workspace_bytes
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    _check(lib().fd_decode_paged_int4(B, Hq, Hkv, D, page_size, num_pages,
+                                      ip.ctypes.data_as(ctypes.c_void_p),
+                                      ll.ctypes.data_as(ctypes.c_void_p), _ptr(kv_page_indptr_dev),
+                                      _ptr(kv_last_page_len_dev), _ptr(kv_page_indices_dev), _ptr(q),
+                                      _ptr(_int4_bytes(k_pages_int4, D)),
+                                      _ptr(_int4_bytes(v_pages_int4, D)), _ptr(k_scale),
+                                      _ptr(v_scale), float(scale), _ptr(o), _ptr(lse),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "fd_decode_paged_int4")
+    return o, lse
+
+
 def plan_graph(batch: int, num_qo_heads: int, num_kv_heads: int, head_dim: int,
                max_total_tokens: int, *, num_sms: int = 0, chunk: int = 0) -> PlanInfo:
     """fd_plan_graph: a plan for any kv_indptr of at most max_total_tokens keys
@@ -398,7 +467,7 @@ def get_device_status(workspace, stream=None) -> int:
 __all__ = [
     "PlanInfo", "FdError", "lib", "build", "plan", "plan_work_items", "decode_split", "merge",
     "decode", "decode_static_workspace", "plan_paged", "decode_paged", "decode_fp8",
-    "decode_paged_fp8", "plan_graph", "decode_graph", "merge_states", "get_device_status",
+    "decode_paged_fp8", "decode_int4", "decode_paged_int4", "plan_graph", "decode_graph", "merge_states", "get_device_status",
     "workspace_bytes", "num_sms",
     "status_string",
     "TILE_TOKENS", "WORKSPACE_HEADER_BYTES", "DEFAULT_TIMEOUT_NS",

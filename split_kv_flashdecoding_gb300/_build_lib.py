@@ -19,8 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfd.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["split_kernel.cu", "split_kernel_fp8.cu", "merge_kernel.cu", "fd_api.cu",
-                "fd_static_ws.cu"]
+CUDA_SOURCES = ["split_kernel.cu", "split_kernel_fp8.cu", "split_kernel_int4.cu", "merge_kernel.cu",
+                "fd_api.cu", "fd_static_ws.cu"]
 HOST_SOURCES = ["plan.cpp"]
 
 

@@ -120,6 +120,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 1-D tiled TMA load of the box starting at element x (x * element size a
+// multiple of 16 bytes) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2}], [%3], %4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // 3-D tiled TMA load of box (x, y, z) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t x,
                                             int32_t y, int32_t z, uint32_t bar, uint64_t policy)

@@ -92,6 +92,43 @@ int make_kv_map_fp8(CUtensorMap *map, const void *base, int64_t rows, int num_kv
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
 }
 
+// INT4 K or V [rows, Hkv, 64] (two four-bit codes per byte) as a 2-D tensor of
+// rows x Hkv*64 bytes; one box = box_rows rows x the head's 64 bytes, 64-byte
+// swizzle, zero fill past the last row.
+int make_kv_map_int4(CUtensorMap *map, const void *base, int64_t rows, int num_kv_heads, int box_rows)
+{
+    auto encode = tensor_map_encoder();
+    if (!encode)
+        return FD_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * kHeadDim / 2, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * kHeadDim / 2};
+    const cuuint32_t box[2] = {kHeadDim / 2, (cuuint32_t)box_rows};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                              strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
+}
+
+// INT4 scales [Hkv][rows] fp32 as a 1-D tensor of Hkv*rows entries; one box =
+// `box` entries, zero fill past the end.
+int make_scale_map(CUtensorMap *map, const float *base, int64_t entries, int box)
+{
+    auto encode = tensor_map_encoder();
+    if (!encode)
+        return FD_ERR_CUDA;
+    const cuuint64_t dims[1] = {(cuuint64_t)entries};
+    const cuuint64_t strides[1] = {0};   // rank 1: no strides are read
+    const cuuint32_t boxdim[1] = {(cuuint32_t)box};
+    const cuuint32_t elem_strides[1] = {1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float *>(base),
+                              dims, strides, boxdim, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
+}
+
 int check_info(const fd_plan_info *info)
 {
     if (!info)
@@ -161,8 +198,10 @@ extern "C" int fd_num_sms(int device, int *num_sms)
 
 namespace {
 
-// FP8 (E4M3) K/V: the per-KV-head scales (device, [Hkv] each).
-struct Fp8KV {
+// Quantised K/V: the element type (fd::kKvTypeFp8 or fd::kKvTypeInt4) and the
+// device scales -- FP8: [Hkv] each; INT4: [Hkv][rows] each.
+struct QuantKV {
+    int type;
     const float *k_scale;
     const float *v_scale;
 };
@@ -186,7 +225,7 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
                   const int32_t *kv_indptr_dev, float scale, float *partial_o, float *partial_lse,
                   void *workspace, float *o, float *lse, int *counters,
                   const int32_t *kv_indptr_host, cudaStream_t stream,
-                  const PagedKV *paged = nullptr, const Fp8KV *fp8 = nullptr,
+                  const PagedKV *paged = nullptr, const QuantKV *quant = nullptr,
                   bool device_plan = false)
 {
     if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
@@ -196,21 +235,41 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
         return FD_ERR_INVALID_ARG;
     if (!(scale == scale))
         return FD_ERR_INVALID_ARG;
-    if (fp8 && (!fp8->k_scale || !fp8->v_scale || !aligned(fp8->k_scale, 4) ||
-                !aligned(fp8->v_scale, 4)))
+    const int kv_type = quant ? quant->type : fd::kKvTypeBf16;
+    const bool int4 = kv_type == fd::kKvTypeInt4;
+    // INT4 scales are read by 16-byte TMA boxes; FP8 scales by plain loads
+    if (quant && (!quant->k_scale || !quant->v_scale || !aligned(quant->k_scale, int4 ? 16 : 4) ||
+                  !aligned(quant->v_scale, int4 ? 16 : 4)))
         return FD_ERR_INVALID_ARG;
 
-    CUtensorMap tm_k, tm_v;
+    fd::KvMaps maps;
     int rc;
     const int64_t rows = paged ? (int64_t)paged->num_pages * paged->page_size : info->total_tokens;
     const int box_rows = paged && paged->page_size % kBoxRows != 0 ? 16 : kBoxRows;
-    if (fp8) {
-        if ((rc = make_kv_map_fp8(&tm_k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
-            (rc = make_kv_map_fp8(&tm_v, v, rows, info->num_kv_heads, box_rows)) != FD_OK)
+    if (kv_type == fd::kKvTypeFp8) {
+        if ((rc = make_kv_map_fp8(&maps.k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+            (rc = make_kv_map_fp8(&maps.v, v, rows, info->num_kv_heads, box_rows)) != FD_OK)
             return rc;
-    } else if ((rc = make_kv_map(&tm_k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
-               (rc = make_kv_map(&tm_v, v, rows, info->num_kv_heads, box_rows)) != FD_OK) {
+    } else if (int4) {
+        // the scale boxes start at element kvh * rows + row: a 32-bit coordinate
+        if ((int64_t)info->num_kv_heads * rows > INT32_MAX - 64)
+            return FD_ERR_UNSUPPORTED;
+        // ragged rows start anywhere: a box of 36 covers 32 scales from the
+        // 16-byte boundary at or below the first; page rows start on one
+        const int scale_box = paged ? box_rows : kBoxRows + 4;
+        const int64_t entries = (int64_t)info->num_kv_heads * rows;
+        if ((rc = make_kv_map_int4(&maps.k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+            (rc = make_kv_map_int4(&maps.v, v, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+            (rc = make_scale_map(&maps.ks, quant->k_scale, entries, scale_box)) != FD_OK ||
+            (rc = make_scale_map(&maps.vs, quant->v_scale, entries, scale_box)) != FD_OK)
+            return rc;
+    } else if ((rc = make_kv_map(&maps.k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+               (rc = make_kv_map(&maps.v, v, rows, info->num_kv_heads, box_rows)) != FD_OK) {
         return rc;
+    }
+    if (!int4) {
+        maps.ks = maps.k;
+        maps.vs = maps.v;
     }
 
     fd::SplitParams p;
@@ -250,14 +309,15 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.num_page_entries = paged ? paged->num_page_entries : 0;
     if (paged && p.indptr_in_params)
         memcpy(p.last_len_param, paged->last_len_host, (size_t)info->batch * sizeof(int32_t));
-    p.kv_fp8 = fp8 != nullptr;
-    p.k_scale = fp8 ? fp8->k_scale : nullptr;
-    p.v_scale = fp8 ? fp8->v_scale : nullptr;
+    p.kv_type = kv_type;
+    p.kv_rows = (int32_t)rows;
+    p.k_scale = quant ? quant->k_scale : nullptr;
+    p.v_scale = quant ? quant->v_scale : nullptr;
     // Persistent grid: at most one wave of resident CTAs on the plan's SMs.
     p.num_work = info->num_work;
     const int64_t slots = (int64_t)info->num_sms * fd::split_ctas_per_sm();
     const int num_ctas = slots > 0 && slots < info->num_work ? (int)slots : info->num_work;
-    const cudaError_t e = fd::launch_split(tm_k, tm_v, p, info->group_size, num_ctas, stream);
+    const cudaError_t e = fd::launch_split(maps, p, info->group_size, num_ctas, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
@@ -315,11 +375,11 @@ extern "C" int fd_merge(const fd_plan_info *info, const int32_t *kv_indptr_dev,
 
 namespace {
 
-// fd_decode and fd_decode_fp8 (fp8 non-null).
+// fd_decode, fd_decode_fp8 and fd_decode_int4 (quant non-null).
 int decode_ragged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                   const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev, const void *q,
                   const void *k, const void *v, float scale, float *o, float *lse, void *workspace,
-                  int64_t workspace_bytes, void *stream, const Fp8KV *fp8)
+                  int64_t workspace_bytes, void *stream, const QuantKV *quant)
 {
     fd_plan_info info;
     int rc = fd_plan(batch, num_qo_heads, num_kv_heads, head_dim, kv_indptr_host, 0, 0, 0, &info);
@@ -341,7 +401,7 @@ int decode_ragged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
     cudaStream_t s = as_stream(stream);
     if (info.num_work > 0) {
         rc = launch_stage1(&info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
-                           o, lse, counters, kv_indptr_host, s, nullptr, fp8);
+                           o, lse, counters, kv_indptr_host, s, nullptr, quant);
         if (rc != FD_OK)
             return rc;
     }
@@ -414,13 +474,14 @@ extern "C" int fd_plan_paged(int batch, int num_qo_heads, int num_kv_heads, int 
 
 namespace {
 
-// fd_decode_paged and fd_decode_paged_fp8 (fp8 non-null).
+// fd_decode_paged, fd_decode_paged_fp8 and fd_decode_paged_int4 (quant non-null).
 int decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
                  int num_pages, const int32_t *kv_page_indptr_host,
                  const int32_t *kv_last_page_len_host, const int32_t *kv_page_indptr_dev,
                  const int32_t *kv_last_page_len_dev, const int32_t *kv_page_indices_dev,
                  const void *q, const void *k_pages, const void *v_pages, float scale, float *o,
-                 float *lse, void *workspace, int64_t workspace_bytes, void *stream, const Fp8KV *fp8)
+                 float *lse, void *workspace, int64_t workspace_bytes, void *stream,
+                 const QuantKV *quant)
 {
     fd_plan_info info;
     int rc = fd_plan_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size,
@@ -448,7 +509,8 @@ int decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim, in
         const PagedKV pk{page_size, num_pages, kv_last_page_len_dev, kv_last_page_len_host,
                          kv_page_indices_dev, kv_page_indptr_host[batch]};
         rc = launch_stage1(&info, q, k_pages, v_pages, kv_page_indptr_dev, scale, partial_o,
-                           partial_lse, workspace, o, lse, counters, kv_page_indptr_host, s, &pk, fp8);
+                           partial_lse, workspace, o, lse, counters, kv_page_indptr_host, s, &pk,
+                           quant);
         if (rc != FD_OK)
             return rc;
     }
@@ -491,9 +553,20 @@ extern "C" int fd_decode_fp8(int batch, int num_qo_heads, int num_kv_heads, int 
                              const float *k_scale, const float *v_scale, float scale, float *o,
                              float *lse, void *workspace, int64_t workspace_bytes, void *stream)
 {
-    const Fp8KV f{k_scale, v_scale};
+    const QuantKV f{fd::kKvTypeFp8, k_scale, v_scale};
     return decode_ragged(batch, num_qo_heads, num_kv_heads, head_dim, kv_indptr_host, kv_indptr_dev,
                          q, k_fp8, v_fp8, scale, o, lse, workspace, workspace_bytes, stream, &f);
+}
+
+extern "C" int fd_decode_int4(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                              const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,
+                              const void *q, const void *k_int4, const void *v_int4,
+                              const float *k_scale, const float *v_scale, float scale, float *o,
+                              float *lse, void *workspace, int64_t workspace_bytes, void *stream)
+{
+    const QuantKV f{fd::kKvTypeInt4, k_scale, v_scale};
+    return decode_ragged(batch, num_qo_heads, num_kv_heads, head_dim, kv_indptr_host, kv_indptr_dev,
+                         q, k_int4, v_int4, scale, o, lse, workspace, workspace_bytes, stream, &f);
 }
 
 extern "C" int fd_decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
@@ -522,10 +595,29 @@ extern "C" int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads
                                    float *o, float *lse, void *workspace, int64_t workspace_bytes,
                                    void *stream)
 {
-    const Fp8KV f{k_scale, v_scale};
+    const QuantKV f{fd::kKvTypeFp8, k_scale, v_scale};
     return decode_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
                         kv_page_indptr_host, kv_last_page_len_host, kv_page_indptr_dev,
                         kv_last_page_len_dev, kv_page_indices_dev, q, k_pages_fp8, v_pages_fp8,
+                        scale, o, lse, workspace, workspace_bytes, stream, &f);
+}
+
+extern "C" int fd_decode_paged_int4(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                                    int page_size, int num_pages,
+                                    const int32_t *kv_page_indptr_host,
+                                    const int32_t *kv_last_page_len_host,
+                                    const int32_t *kv_page_indptr_dev,
+                                    const int32_t *kv_last_page_len_dev,
+                                    const int32_t *kv_page_indices_dev, const void *q,
+                                    const void *k_pages_int4, const void *v_pages_int4,
+                                    const float *k_scale, const float *v_scale, float scale,
+                                    float *o, float *lse, void *workspace, int64_t workspace_bytes,
+                                    void *stream)
+{
+    const QuantKV f{fd::kKvTypeInt4, k_scale, v_scale};
+    return decode_paged(batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
+                        kv_page_indptr_host, kv_last_page_len_host, kv_page_indptr_dev,
+                        kv_last_page_len_dev, kv_page_indices_dev, q, k_pages_int4, v_pages_int4,
                         scale, o, lse, workspace, workspace_bytes, stream, &f);
 }
 

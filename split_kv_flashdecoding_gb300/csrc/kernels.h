@@ -53,11 +53,25 @@ struct SplitParams {
     int32_t num_pages;
     int32_t num_page_entries;   // kv_indptr[B]
     int32_t last_len_param[kParamIndptr];
-    // FP8 (E4M3) K/V: one byte per element, dequantised in registers; k_scale,
-    // v_scale [Hkv] (device) multiply the head's K and V values.
-    int32_t kv_fp8;
+    // Element type of K/V (kKvTypeBf16, kKvTypeFp8, kKvTypeInt4), dequantised in
+    // registers.  FP8 (E4M3): one byte per element; k_scale, v_scale [Hkv]
+    // (device) multiply the head's K and V values.  INT4: two four-bit codes
+    // per byte, and one scale per key row and head, read through the scale
+    // tensor maps ([Hkv][kv_rows] fp32).
+    int32_t kv_type;
+    int32_t kv_rows;            // rows of K/V: T keys, or num_pages * page_size
     const float *k_scale;
     const float *v_scale;
+};
+
+constexpr int kKvTypeBf16 = 0;
+constexpr int kKvTypeFp8 = 1;
+constexpr int kKvTypeInt4 = 2;
+
+// The split kernel's TMA descriptors: K and V, and (INT4) the K and V scales;
+// for the other types ks / vs repeat k / v and are not read.
+struct KvMaps {
+    CUtensorMap k, v, ks, vs;
 };
 
 struct MergeParams {
@@ -80,12 +94,14 @@ struct MergeParams {
 // CTAs (1 <= num_ctas <= p.num_work), CTA c taking items c, c + num_ctas, ...
 // Launched as a programmatic dependent of the preceding grid (it waits for
 // that grid before touching global memory).
-cudaError_t launch_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
-                         int group, int num_ctas, cudaStream_t stream);
+cudaError_t launch_split(const KvMaps &maps, const SplitParams &p, int group, int num_ctas,
+                         cudaStream_t stream);
 
-// The same for FP8 K/V (p.kv_fp8 set); launch_split dispatches to it.
-cudaError_t launch_split_fp8(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
-                             int group, int num_ctas, cudaStream_t stream);
+// The same for FP8 and INT4 K/V (p.kv_type); launch_split dispatches to them.
+cudaError_t launch_split_fp8(const KvMaps &maps, const SplitParams &p, int group, int num_ctas,
+                             cudaStream_t stream);
+cudaError_t launch_split_int4(const KvMaps &maps, const SplitParams &p, int group, int num_ctas,
+                              cudaStream_t stream);
 
 // Resident split-kernel CTAs per SM the launch shape is built for.
 int split_ctas_per_sm();

@@ -62,7 +62,7 @@ namespace {
 constexpr int kHalfBytes = kTile * 128;   // 32 keys x 64 bf16
 
 enum KvLayout { kKvRagged = 0, kKvPaged = 1, kKvPaged16 = 2 };
-enum KvType { kKvBf16 = 0, kKvFp8 = 1 };
+enum KvType { kKvBf16 = 0, kKvFp8 = 1, kKvInt4 = 2 };
 
 // One pipeline stage holds K then V for kTile = 32 keys of one KV head.
 //  bf16: a tensor's key row r (0..31), column half h (64 columns of 128 bytes,
@@ -74,12 +74,32 @@ enum KvType { kKvBf16 = 0, kKvFp8 = 1 };
 //  FP8: a tensor is [32 rows][128 bytes] (a key row of the head is 128 one-byte
 //    values), 16-byte chunks XOR-swizzled by r % 8; a second 16-row page box
 //    lands 16 rows further.
+//  INT4: a tensor is [32 rows][64 bytes] (128 four-bit values), 16-byte chunks
+//    XOR-swizzled by (r / 2) % 4 (the 64-byte swizzle), then the rows' K scales
+//    and V scales (fp32), each in a 256-byte slot: one box of kScaleBox scales
+//    per 32 rows (ragged: from the 16-byte boundary at or below the tile's
+//    first scale, so the tile's scales start srem = 0..3 entries in), or for
+//    16-row pages two boxes of 16, the second 128 bytes in (kScaleGap bytes
+//    after the first box's end).  Every copy lands on a 128-byte boundary, and
+//    the stage stride is a multiple of 512 bytes, the swizzle's period.
 template <int KV, int DT>
 struct Stage {
     static constexpr bool kFp8 = DT == kKvFp8;
-    static constexpr int kTensorBytes = kFp8 ? kTile * 128 : 2 * kHalfBytes;
-    static constexpr int kBytes = 2 * kTensorBytes;
+    static constexpr bool kInt4 = DT == kKvInt4;
+    static constexpr int kTensorBytes = kInt4 ? kTile * 64 : kFp8 ? kTile * 128 : 2 * kHalfBytes;
     static constexpr int kBoxRows = KV == kKvPaged16 ? 16 : kTile;
+    static constexpr int kScaleBox = KV == kKvRagged ? kTile + 4 : kBoxRows;   // fp32 entries
+    static constexpr int kKsOff = 2 * kTensorBytes;
+    static constexpr int kVsOff = kKsOff + 256;
+    static constexpr int kScaleGap = KV == kKvPaged16 ? 128 - 16 * 4 : 0;
+    static constexpr int kScaleTx = kInt4 ? 2 * (kTile / kBoxRows) * kScaleBox * 4 : 0;
+    static constexpr int kTxBytes = 2 * kTensorBytes + kScaleTx;   // bytes one stage's copies bring
+    static constexpr int kBytes = kInt4 ? (kVsOff + 256 + 511) / 512 * 512 : 2 * kTensorBytes;
+    // a tensor copy's shared-memory destination must be 128-byte aligned
+    static_assert(kTensorBytes % 512 == 0 && kKsOff % 128 == 0 && kVsOff % 128 == 0 &&
+                      kBytes % 512 == 0, "stage copies on 128-byte boundaries");
+    static_assert(!kInt4 || (kBoxRows == kTile ? kScaleBox * 4 : 128 + kScaleBox * 4) <= 256,
+                  "the scale boxes fit their 256-byte slot");
     static constexpr int kHalfStride = KV == kKvPaged16 ? 2048 : kHalfBytes;
     static constexpr int kBlockStride = KV == kKvPaged16 ? 4096 : 2048;
 };
@@ -91,21 +111,22 @@ enum Misc { kAbort, kIssued, kDescs, kLast, kFinalK, kMiscCount };
 // warps: request, its split prefix and count, split, key range [t0, t1)
 // relative to the request's first key, KV head, index of the item's first
 // tile in the CTA's stream of tiles, the head's K and V scales (FP8 K/V; float
-// bits), and a state: kItemOk, kItemBad (outside
-// the plan: the CTA stops) or kItemEnd (no further item; the previous one was
-// the CTA's last).
-enum Desc { kDB, kDPrefix, kDSplits, kDS, kDT0, kDT1, kDKvh, kDGt0, kDState, kDKs, kDVs, kDescInts };
+// bits), where the tiles' scales start in their stage (INT4 K/V: srem), and a
+// state: kItemOk, kItemBad (outside the plan: the CTA stops) or kItemEnd (no
+// further item; the previous one was the CTA's last).
+enum Desc { kDB, kDPrefix, kDSplits, kDS, kDT0, kDT1, kDKvh, kDGt0, kDState, kDKs, kDVs, kDSrem,
+            kDescInts };
 enum ItemState { kItemBad = 0, kItemOk = 1, kItemEnd = 2 };
 constexpr int kDescSlots = 4;
 
 struct Item {
-    int32_t b, prefix, splits, s, t0, t1, kvh, gt0, state, ks, vs;
+    int32_t b, prefix, splits, s, t0, t1, kvh, gt0, state, ks, vs, srem;
 };
 
 __device__ __forceinline__ Item read_item(const volatile int *d)
 {
     return Item{d[kDB], d[kDPrefix], d[kDSplits], d[kDS], d[kDT0], d[kDT1],
-                d[kDKvh], d[kDGt0], d[kDState], d[kDKs], d[kDVs]};
+                d[kDKvh], d[kDGt0], d[kDState], d[kDKs], d[kDVs], d[kDSrem]};
 }
 
 // Shared memory of the one-item kernel: [stage ring | full[NS] empty[NS] |
@@ -234,6 +255,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem)
 __device__ __forceinline__ float bf16_round(float x)
 {
     return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Eight 4-bit two's-complement values (nibble j of each 16-bit half of x; the
+// low nibble first) -> four bf16x2: r[j] = (nibble j of the low half, nibble j
+// of the high half).  Flipping a code's sign bit gives u = n + 8 in 0..15; the
+// bf16 with bits 0x4300 | u is 128 + u (at 128 the unit in the last place is
+// 1), and subtracting 136 leaves n.  Both steps are exact.
+__device__ __forceinline__ void int4x8_to_bf16x2x4(uint32_t x, uint32_t (&r)[4])
+{
+    constexpr uint32_t kMagic = 0x43084308u;   // (0x4300 | 8) in both halves: 136.0
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t t = ((x >> (4 * j)) & 0x000F000Fu) ^ kMagic;
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r[j]) : "r"(t), "r"(kMagic));
+    }
+}
+
+// One fp32 from shared memory (32-bit shared address).
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
 }
 
 // Stage 2 for one (request, KV head) group, run by the CTA that finished the
@@ -368,10 +412,20 @@ __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, in
 //    same order.  For P V, ldmatrix.trans gives lane (g, t4) dims 16c + 2g and
 //    +1 of keys 2t4 and 2t4+1, so one tile of columns takes the even dims and
 //    one the odd: o_acc[2c + e] holds dims 16c + 4t4 + e (and + 2).
+//  INT4: mma.sync bf16; the four-bit codes are widened to bf16 (exact) in
+//    registers.  An ldmatrix of the 64-byte key rows gives lane (g, t4) dims
+//    32c + 8t4 .. +7 of key g in one word; nibbles j and j + 4 pair up, so
+//    k-step 2c + h takes dims 32c + 8t4 + 2h (+4) at k 2t4 (+1) and + 2h + 1
+//    (+4) at k 2t4 + 8 (+9); qa holds q in that order.  Each key's K scale
+//    multiplies its logit, and its V scale its probability in P V (the row sum
+//    takes the probability alone).  ldmatrix.trans of V gives lane (g, t4) dims
+//    32c + 4g .. +3 of keys 2t4 and 2t4 + 1, so o_acc[4c + j] holds dims
+//    32c + 8t4 + j (and + 4).  The tile's scales start srem entries into the
+//    stage's scale boxes.
 template <int KV, int DT>
 __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uint32_t (&qa)[8][2],
                                              float qk_scale, int lane, float &m_run, float &l_part,
-                                             float (&o_acc)[16][4])
+                                             float (&o_acc)[16][4], int srem = 0)
 {
     using S = Stage<KV, DT>;
     const int t4 = lane & 3;
@@ -384,7 +438,22 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
 #pragma unroll
     for (int jn = 0; jn < 4; ++jn)
         sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
-    if constexpr (S::kFp8) {
+    if constexpr (S::kInt4) {
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn) {
+            // matrix lm = chunk lm of key rows 8 jn .. +7 (64-byte swizzle)
+            const int r = 8 * jn + lr;
+            uint32_t kb[4];
+            ldsm_x4(st + r * 64 + ((lm ^ ((r >> 1) & 3)) << 4), kb);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t b[4];   // b[j]: dims 32c + 8t4 + j and + 4 of key 8 jn + g
+                int4x8_to_bf16x2x4(kb[c], b);
+                mma_bf16(sc[jn], qa[2 * c][0], 0u, qa[2 * c][1], 0u, b[0], b[1]);
+                mma_bf16(sc[jn], qa[2 * c + 1][0], 0u, qa[2 * c + 1][1], 0u, b[2], b[3]);
+            }
+        }
+    } else if constexpr (S::kFp8) {
 #pragma unroll
         for (int jn = 0; jn < 4; ++jn) {
 #pragma unroll
@@ -420,12 +489,17 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
     // ---- online softmax on row g_row (this thread's 8 scores of the tile)
     float x[8];
     float mt = -INFINITY;
+    const uint32_t ks_base = st + S::kKsOff + 4 * srem, vs_base = st + S::kVsOff + 4 * srem;
 #pragma unroll
     for (int jn = 0; jn < 4; ++jn)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int key = 8 * jn + 2 * t4 + e;
-            const float v = key < n_valid ? sc[jn][e] * qk_scale : -INFINITY;
+            float logit = sc[jn][e] * qk_scale;
+            if constexpr (S::kInt4)   // keys 16..31 sit kScaleGap further (16-row pages)
+                logit = sc[jn][e] * lds_f32(ks_base + 4 * key + (jn >= 2 ? S::kScaleGap : 0)) *
+                        qk_scale;
+            const float v = key < n_valid ? logit : -INFINITY;
             x[2 * jn + e] = v;
             mt = fmaxf(mt, v);
         }
@@ -455,8 +529,18 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
     uint32_t pa[2][4];
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const float p0 = x[4 * ks], p1 = x[4 * ks + 1];
-        const float p2 = x[4 * ks + 2], p3 = x[4 * ks + 3];
+        float p0 = x[4 * ks], p1 = x[4 * ks + 1];
+        float p2 = x[4 * ks + 2], p3 = x[4 * ks + 3];
+        if constexpr (S::kInt4) {
+            // keys 16ks + 2t4 (+1) and 16ks + 8 + 2t4 (+1); a masked key's
+            // scale (another request's row, or past the end) is not read
+            const int k0 = 16 * ks + 2 * t4;
+            const uint32_t vk = vs_base + 4 * k0 + ks * S::kScaleGap;
+            p0 = k0 < n_valid ? p0 * lds_f32(vk) : 0.f;
+            p1 = k0 + 1 < n_valid ? p1 * lds_f32(vk + 4) : 0.f;
+            p2 = k0 + 8 < n_valid ? p2 * lds_f32(vk + 32) : 0.f;
+            p3 = k0 + 9 < n_valid ? p3 * lds_f32(vk + 36) : 0.f;
+        }
         if constexpr (S::kFp8) {
             const float h0 = f16_round(p0), h1 = f16_round(p1);
             const float h2 = f16_round(p2), h3 = f16_round(p3);
@@ -475,7 +559,30 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
     }
 
     // ---- O += P V : 2 k-steps of 16 keys, 16 n-tiles of 8 columns
-    if constexpr (S::kFp8) {
+    if constexpr (S::kInt4) {
+        const uint32_t vt = st + S::kTensorBytes;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            // matrix lm: keys 16 ks + 8 (lm & 1) .. +7, chunk 2 cp + (lm >> 1)
+            const int r = 16 * ks + 8 * (lm & 1) + lr;
+#pragma unroll
+            for (int cp = 0; cp < 2; ++cp) {
+                uint32_t vb[4];
+                ldsm_x4_trans(vt + r * 64 + (((2 * cp + (lm >> 1)) ^ ((r >> 1) & 3)) << 4), vb);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {         // chunk c = 2 cp + h: vb[2h] keys +0..7, vb[2h+1] +8..15
+                    const int c = 2 * cp + h;
+                    uint32_t lo[4], hi[4];            // [j]: dim 32c + 4g + j of keys 2t4, 2t4 + 1
+                    int4x8_to_bf16x2x4(vb[2 * h], lo);
+                    int4x8_to_bf16x2x4(vb[2 * h + 1], hi);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_bf16(o_acc[4 * c + j], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], lo[j],
+                                 hi[j]);
+                }
+            }
+        }
+    } else if constexpr (S::kFp8) {
         const uint32_t vt = st + S::kTensorBytes;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
@@ -529,6 +636,7 @@ struct TileSource {
     static constexpr bool kPaged = KV != kKvRagged;
     const SplitParams &p;
     const CUtensorMap *tm_k, *tm_v;
+    const CUtensorMap *tm_ks, *tm_vs;   // INT4: the K and V scales
     uint8_t *ring;
     uint64_t *full;   // full[NS]
     uint64_t pol;
@@ -543,9 +651,11 @@ struct TileSource {
     int32_t cur_pg = 0, cur_off = 0;
 
     __device__ __forceinline__ TileSource(const SplitParams &p_, const CUtensorMap *k,
-                                          const CUtensorMap *v, uint8_t *ring_, uint64_t *full_,
+                                          const CUtensorMap *v, const CUtensorMap *ks,
+                                          const CUtensorMap *vs, uint8_t *ring_, uint64_t *full_,
                                           int lane_)
-        : p(p_), tm_k(k), tm_v(v), ring(ring_), full(full_), pol(l2_evict_first_policy()), lane(lane_)
+        : p(p_), tm_k(k), tm_v(v), tm_ks(ks), tm_vs(vs), ring(ring_), full(full_),
+          pol(l2_evict_first_policy()), lane(lane_)
     {
     }
 
@@ -616,14 +726,28 @@ struct TileSource {
 
     // Put stream tile g (KV head kvh) into stage g % NS, per tensor and per box
     // of rows: bf16, one 3-D box of both 64-column halves; FP8, one 2-D box of
-    // the rows' 128 bytes.
+    // the rows' 128 bytes; INT4, one 2-D box of the rows' 64 bytes and a 1-D
+    // box of their scales (from the 16-byte boundary at or below the first).
     __device__ __forceinline__ void issue(int g, int kvh, int32_t ya, int32_t yb) const
     {
         const int s = g % NS;
         const uint32_t bar = smem_addr(&full[s]);
         const uint32_t dst = smem_addr(ring + s * SL::kBytes);
-        mbar_arrive_expect_tx(bar, SL::kBytes);
-        if constexpr (SL::kFp8) {
+        mbar_arrive_expect_tx(bar, SL::kTxBytes);
+        if constexpr (SL::kInt4) {
+            const int32_t x = kvh * (kHeadDim / 2);
+            const int32_t head_rows = kvh * p.kv_rows;   // the head's first scale
+            tma_load_2d(dst, tm_k, x, ya, bar, pol);
+            tma_load_2d(dst + SL::kTensorBytes, tm_v, x, ya, bar, pol);
+            tma_load_1d(dst + SL::kKsOff, tm_ks, (head_rows + ya) & ~3, bar, pol);
+            tma_load_1d(dst + SL::kVsOff, tm_vs, (head_rows + ya) & ~3, bar, pol);
+            if constexpr (SL::kBoxRows < kTile) {
+                tma_load_2d(dst + 16 * 64, tm_k, x, yb, bar, pol);
+                tma_load_2d(dst + SL::kTensorBytes + 16 * 64, tm_v, x, yb, bar, pol);
+                tma_load_1d(dst + SL::kKsOff + 128, tm_ks, (head_rows + yb) & ~3, bar, pol);
+                tma_load_1d(dst + SL::kVsOff + 128, tm_vs, (head_rows + yb) & ~3, bar, pol);
+            }
+        } else if constexpr (SL::kFp8) {
             const int32_t x = kvh * kHeadDim;
             tma_load_2d(dst, tm_k, x, ya, bar, pol);
             tma_load_2d(dst + SL::kTensorBytes, tm_v, x, ya, bar, pol);
@@ -664,8 +788,9 @@ __device__ __forceinline__ bool item_range(const SplitParams &p, const SplitCoor
 
 __device__ __forceinline__ void write_desc(volatile int *d, const SplitCoord &c, int32_t t0,
                                            int32_t t1, int kvh, int gt0, int state, float ks = 1.f,
-                                           float vs = 1.f)
+                                           float vs = 1.f, int srem = 0)
 {
+    d[kDSrem] = srem;
     d[kDKs] = __float_as_int(ks);
     d[kDVs] = __float_as_int(vs);
     d[kDB] = c.b;
@@ -677,6 +802,19 @@ __device__ __forceinline__ void write_desc(volatile int *d, const SplitCoord &c,
     d[kDKvh] = kvh;
     d[kDGt0] = gt0;
     d[kDState] = state;
+}
+
+// INT4 K/V: where an item's tile scales start in their stage.  A ragged item's
+// tiles start at key rows base + t0 + 32i, so their scales (head kvh's entries
+// at kvh * kv_rows + row) all sit (kvh * kv_rows + base + t0) % 4 entries past
+// a 16-byte boundary; page rows start on one (page_size and kv_rows are
+// multiples of 16).
+template <int KV, int DT>
+__device__ __forceinline__ int scale_rem(const SplitParams &p, int kvh, int32_t base, int32_t t0)
+{
+    if constexpr (DT == kKvInt4 && KV == kKvRagged)
+        return (kvh * p.kv_rows + base + t0) & 3;
+    return 0;
 }
 
 __device__ __forceinline__ KeyIndex key_index(const SplitParams &p, bool paged)
@@ -694,12 +832,32 @@ __device__ __forceinline__ KeyIndex key_index(const SplitParams &p, bool paged)
 //    that puts its largest magnitude in [2^8, 2^9), so every bf16 value of the
 //    row converts to f16 exactly (values below 2^-22 of the row's maximum
 //    round in f16's subnormal range); returns the inverse power.
+//  INT4 (bf16 MMA): qa[2c + h] = dims 32c + 8t4 + 2h (+4) and 32c + 8t4 + 2h + 1
+//    (+4), the order consume_tile reads K in; 1.
 template <int G, int DT, bool GLOBAL>
 __device__ __forceinline__ float load_q(const uint16_t *qrows, int lane, uint32_t (&qa)[8][2])
 {
     const int g_row = lane >> 2, t4 = lane & 3;
     const bool valid = g_row < G;
-    if constexpr (DT == kKvFp8) {
+    if constexpr (DT == kKvInt4) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(qrows + (valid ? g_row : 0) * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);   // dims 32c + 8t4 .. +7
+            if constexpr (GLOBAL) {
+                if (valid)
+                    raw = __ldg(row + 4 * c + t4);
+            } else {
+                if (valid)
+                    raw = row[4 * c + t4];
+            }
+            qa[2 * c][0] = __byte_perm(raw.x, raw.z, 0x5410);       // dims +0, +4
+            qa[2 * c][1] = __byte_perm(raw.x, raw.z, 0x7632);       // dims +1, +5
+            qa[2 * c + 1][0] = __byte_perm(raw.y, raw.w, 0x5410);   // dims +2, +6
+            qa[2 * c + 1][1] = __byte_perm(raw.y, raw.w, 0x7632);   // dims +3, +7
+        }
+        return 1.f;
+    } else if constexpr (DT == kKvFp8) {
         const uint2 *row = reinterpret_cast<const uint2 *>(qrows + (valid ? g_row : 0) * kHeadDim);
         uint2 raw[8];
         float amax = 0.f;
@@ -746,7 +904,8 @@ __device__ __forceinline__ float load_q(const uint16_t *qrows, int lane, uint32_
 
 // Consumer warp `warp`: put its online-softmax state for one item (O rows g
 // and g+8 summed and multiplied by vscale, running max, row sum) into a state
-// buffer, O in dim order (consume_tile's FP8 column order is undone here).
+// buffer, O in dim order (consume_tile's FP8 and INT4 column orders are undone
+// here).
 template <int G, int NC, int DT>
 __device__ __forceinline__ void write_state(uint8_t *state, int warp, int lane,
                                             const float (&o_acc)[16][4], float m_run, float l_part,
@@ -760,7 +919,19 @@ __device__ __forceinline__ void write_state(uint8_t *state, int warp, int lane,
     l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
     l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
     if (g_row < G) {
-        if constexpr (DT == kKvFp8) {
+        if constexpr (DT == kKvInt4) {
+            float *dst = comb_acc + (warp * G + g_row) * kHeadDim + 8 * t4;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {   // dims 32c + 8t4 + (0..3), then + (4..7)
+                const int n = 4 * c;
+                *reinterpret_cast<float4 *>(dst + 32 * c) = make_float4(
+                    o_acc[n][0] + o_acc[n][2], o_acc[n + 1][0] + o_acc[n + 1][2],
+                    o_acc[n + 2][0] + o_acc[n + 2][2], o_acc[n + 3][0] + o_acc[n + 3][2]);
+                *reinterpret_cast<float4 *>(dst + 32 * c + 4) = make_float4(
+                    o_acc[n][1] + o_acc[n][3], o_acc[n + 1][1] + o_acc[n + 1][3],
+                    o_acc[n + 2][1] + o_acc[n + 2][3], o_acc[n + 3][1] + o_acc[n + 3][3]);
+            }
+        } else if constexpr (DT == kKvFp8) {
             float *dst = comb_acc + (warp * G + g_row) * kHeadDim + 4 * t4;
 #pragma unroll
             for (int c = 0; c < 8; ++c)   // dims 16c + 4t4 + (0, 1, 2, 3)
@@ -869,6 +1040,8 @@ template <int G, int NC, int NS, int MIN_CTAS, int KV, int DT>
 __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     split_kv_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_ks,
+                    const __grid_constant__ CUtensorMap tm_vs,
                     const __grid_constant__ SplitParams p)
 {
     using SG = Stage<KV, DT>;
@@ -914,7 +1087,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         // past the batch's items have nothing to do
         const bool none = !found && p.device_plan;
         if (lane == 0) {
-            write_desc(desc, c, t0, t1, kvh, 0, ok ? kItemOk : (none ? kItemEnd : kItemBad));
+            write_desc(desc, c, t0, t1, kvh, 0, ok ? kItemOk : (none ? kItemEnd : kItemBad), 1.f,
+                       1.f, scale_rem<KV, DT>(p, kvh, c.base, t0));
             misc[kAbort] = ok || none ? 0 : 1;
             misc[kIssued] = 0;
             misc[kLast] = 0;
@@ -927,7 +1101,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                 report(p.status, FD_ERR_DEVICE_BOUNDS);
         }
         __syncwarp();
-        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
+        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, &tm_ks, &tm_vs, smem, bars, lane);
         const int n_tiles = ok ? (t1 - t0 + kTile - 1) / kTile : 0;
         const int first = min(NS, n_tiles);
         if (ok && (paged || lane == 0)) {
@@ -992,7 +1166,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                     break;
                 }
                 consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc);
+                                     qk, lane, m_run, l_part, o_acc, it.srem);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1039,6 +1213,8 @@ template <int G, int NC, int NS, int MIN_CTAS, int KV, int DT>
 __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
     split_kv_persistent_kernel(const __grid_constant__ CUtensorMap tm_k,
                                const __grid_constant__ CUtensorMap tm_v,
+                               const __grid_constant__ CUtensorMap tm_ks,
+                               const __grid_constant__ CUtensorMap tm_vs,
                                const __grid_constant__ SplitParams p)
 {
     using SG = Stage<KV, DT>;
@@ -1101,7 +1277,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
         const KeyIndex ki = key_index(p, paged);
         SplitCursor cursor;
         cursor.empty_split = p.device_plan;
-        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
+        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, &tm_ks, &tm_vs, smem, bars, lane);
         int gt = 0;      // tiles issued so far (index of the stream's next tile)
         int descs = 0;   // descriptors published (lane 0)
 
@@ -1206,7 +1382,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                         vs = __ldg(p.v_scale + kvh);
                     }
                     write_desc(desc + slot * kDescInts, c, t0, t1, kvh, gt, ok ? kItemOk : kItemBad,
-                               ks, vs);
+                               ks, vs, scale_rem<KV, DT>(p, kvh, c.base, t0));
                     ++descs;
                     const uint32_t fb = smem_addr(&item_full[slot]);
                     if (ok) {
@@ -1277,7 +1453,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                     break;
                 }
                 consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc);
+                                     qk, lane, m_run, l_part, o_acc, it.srem);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1401,8 +1577,7 @@ constexpr int kMinCtas = FD_SPLIT_CTAS_PER_SM;
 // dynamic shared memory once per device (for the first 64 devices).
 template <typename Kernel>
 cudaError_t launch_kernel(Kernel kern, bool (&configured)[64], int smem_bytes, int threads,
-                          int num_ctas, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const SplitParams &p, cudaStream_t stream)
+                          int num_ctas, const KvMaps &m, const SplitParams &p, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1425,22 +1600,21 @@ cudaError_t launch_kernel(Kernel kern, bool (&configured)[64], int smem_bytes, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, kern, m.k, m.v, m.ks, m.vs, p);
 }
 
-// Stages in the ring: FP8 tiles are half the bytes, so the same 64 KB ring
-// holds twice as many (two per consumer warp).
+// Stages in the ring: FP8 and INT4 tiles are half the bytes or less, so the
+// ring holds twice as many (two per consumer warp).
 template <int DT>
 constexpr int stages_for()
 {
-    return DT == kKvFp8 ? 2 * kNS : kNS;
+    return DT == kKvBf16 ? kNS : 2 * kNS;
 }
 
 // One wave of items: one item per CTA.  More: the persistent kernel on
 // num_ctas CTAs.
 template <int G, int KV, int DT>
-cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitParams &p,
-                     int num_ctas, cudaStream_t stream)
+cudaError_t launch_g(const KvMaps &m, const SplitParams &p, int num_ctas, cudaStream_t stream)
 {
     constexpr int NS = stages_for<DT>();
     using SG = Stage<KV, DT>;
@@ -1451,18 +1625,18 @@ cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const SplitPa
     if (num_ctas >= p.num_work) {   // one wave: one item (or, device-side plan, at most one) per CTA
         static bool configured[64] = {};
         return launch_kernel(split_kv_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured, LS::kAlloc,
-                             LS::kWarps * 32, p.num_work, tk, tv, p, stream);
+                             LS::kWarps * 32, p.num_work, m, p, stream);
     }
     static bool configured[64] = {};
     return launch_kernel(split_kv_persistent_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured,
-                         LP::kAlloc, LP::kWarps * 32, num_ctas, tk, tv, p, stream);
+                         LP::kAlloc, LP::kWarps * 32, num_ctas, m, p, stream);
 }
 
 // Stage 1 for K/V elements of type DT: dispatch on the group size and the KV
 // layout.
 template <int DT>
-cudaError_t launch_split_dt(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
-                            int group, int num_ctas, cudaStream_t stream)
+cudaError_t launch_split_dt(const KvMaps &m, const SplitParams &p, int group, int num_ctas,
+                            cudaStream_t stream)
 {
     if (num_ctas < 1 || num_ctas > p.num_work)
         return cudaErrorInvalidValue;
@@ -1472,9 +1646,9 @@ cudaError_t launch_split_dt(const CUtensorMap &tm_k, const CUtensorMap &tm_v, co
     auto by_layout = [&](auto g) -> cudaError_t {
         constexpr int G = decltype(g)::value;
         switch (kv) {
-        case kKvRagged: return launch_g<G, kKvRagged, DT>(tm_k, tm_v, p, num_ctas, stream);
-        case kKvPaged: return launch_g<G, kKvPaged, DT>(tm_k, tm_v, p, num_ctas, stream);
-        default: return launch_g<G, kKvPaged16, DT>(tm_k, tm_v, p, num_ctas, stream);
+        case kKvRagged: return launch_g<G, kKvRagged, DT>(m, p, num_ctas, stream);
+        case kKvPaged: return launch_g<G, kKvPaged, DT>(m, p, num_ctas, stream);
+        default: return launch_g<G, kKvPaged16, DT>(m, p, num_ctas, stream);
         }
     };
     switch (group) {

@@ -11,10 +11,10 @@
 
 namespace fd {
 
-cudaError_t launch_split_fp8(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const SplitParams &p,
-                             int group, int num_ctas, cudaStream_t stream)
+cudaError_t launch_split_fp8(const KvMaps &maps, const SplitParams &p, int group, int num_ctas,
+                             cudaStream_t stream)
 {
-    return launch_split_dt<kKvFp8>(tm_k, tm_v, p, group, num_ctas, stream);
+    return launch_split_dt<kKvFp8>(maps, p, group, num_ctas, stream);
 }
 
 }  // namespace fd

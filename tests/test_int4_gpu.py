@@ -1,0 +1,147 @@
+"""INT4 KV on the GPU (fd_decode_int4, fd_decode_paged_int4) against the fp64
+oracle on the exactly dequantised K/V (oracle.decode_int4).
+
+FD++ §4 (quantisation-friendly fusion): the packed codes are read as they are
+and dequantised in registers.  The reference result is attention over the
+dequantised values; the tolerances are those of the bf16 path.  Inputs are
+both quantised bf16 (to_int4: codes -7..7, positive scales) and uniformly
+random bytes with signed scales (random_int4: every code -8..7).
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_flashdecoding_gb300 as fd
+from tests.parity_util import assert_within, errors
+from workloads import make_inputs, make_small, random_int4, to_int4, to_paged_int4
+
+pytestmark = pytest.mark.gpu
+
+TIGHT = dict(max_abs=1e-4, rel_l2=1e-5, lse_abs=2e-5)
+
+CASES = [
+    # (name, B, Hq, Hkv, lengths)
+    ("single_key", 1, 4, 4, [1]),
+    ("one_tile_minus_one", 1, 8, 2, [31]),
+    ("ragged_with_empty", 5, 16, 8, [0, 77, 0, 300, 1]),
+    ("several_tiles_g8", 2, 64, 8, [1000, 1537]),
+    ("mha_long", 1, 8, 8, [4099]),
+    ("many_splits", 1, 32, 8, [5000]),          # one wave
+    ("ragged_many", 6, 16, 2, [3000, 0, 17, 900, 4100, 1]),
+    ("odd_offsets", 4, 8, 1, [5, 33, 63, 2049]),  # scale rows start at every offset mod 4
+    ("multi_wave_g8", 2, 64, 8, [9000, 2500]),  # more items than one wave: persistent kernel
+]
+
+KINDS = {"quantised": lambda inp: to_int4(inp), "random": lambda inp: random_int4(inp, seed=21)}
+
+
+def _run(f, dev, ws=None):
+    d = {k: f[k].to(dev) for k in ("q", "k_int4", "v_int4", "k_scale_int4", "v_scale_int4")}
+    ip_dev = f["kv_indptr"].to(dev)
+    return fd.decode_int4(d["q"], d["k_int4"], d["v_int4"], d["k_scale_int4"], d["v_scale_int4"],
+                          f["kv_indptr"], ip_dev, f["scale"], workspace=ws)
+
+
+def _ref(f, rows=None):
+    return oracle.decode_int4(f["q"], f["k_int4"], f["v_int4"], f["k_scale_int4"],
+                              f["v_scale_int4"], f["kv_indptr"], f["scale"], rows=rows)
+
+
+@pytest.mark.parametrize("kind", sorted(KINDS))
+@pytest.mark.parametrize("name,B,Hq,Hkv,lengths", CASES, ids=[c[0] for c in CASES])
+def test_int4_decode_matches_oracle(cuda_device, name, B, Hq, Hkv, lengths, kind):
+    f = KINDS[kind](make_small(B, Hq, Hkv, 128, lengths, seed=zlib.crc32(name.encode()) % 1000))
+    ws = torch.zeros(fd.workspace_bytes(B, Hq, Hkv, 128, f["kv_indptr"]), dtype=torch.uint8,
+                     device=cuda_device)
+    for rep in range(2):   # the second call reuses the workspace (tickets, claim counter)
+        o, lse = _run(f, cuda_device, ws)
+        torch.cuda.synchronize()
+        assert fd.get_device_status(ws) == 0
+    o_ref, lse_ref = _ref(f)
+    err = errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
+    assert_within(err, what=f"{name} {kind}")
+    assert_within(err, **TIGHT, what=f"{name} {kind} (tight)")
+
+
+@pytest.mark.parametrize("idx", [1, 4], ids=["gqa_b1_h32x8_l65536", "stressed_b16_h64x8_l32768"])
+def test_int4_full_size(cuda_device, idx):
+    """Full-size workloads quantised to INT4, in the launch configuration the
+    benchmark uses: sampled rows against the oracle."""
+    inp = make_inputs(idx)
+    f = to_int4(inp)
+    w = inp["workload"]
+    o, lse = _run(f, cuda_device)
+    torch.cuda.synchronize()
+    B, Hq, D = w.batch, w.num_qo_heads, w.head_dim
+    rows = np.random.default_rng(idx).permutation(B * Hq)[:32]
+    o_ref, lse_ref = _ref(f, rows=rows)
+    o_h = o.reshape(B * Hq, D).cpu().numpy()[rows]
+    l_h = lse.reshape(B * Hq).cpu().numpy()[rows]
+    assert_within(errors(o_h, l_h, o_ref, lse_ref), what=w.name)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def _paged_call(pg, f, dev):
+    d = {k: pg[k].to(dev) for k in ("q", "k_pages_int4", "v_pages_int4", "k_scale_pages",
+                                      "v_scale_pages", "kv_page_indptr", "kv_page_indices",
+                                      "kv_last_page_len")}
+    return fd.decode_paged_int4(d["q"], d["k_pages_int4"], d["v_pages_int4"], d["k_scale_pages"],
+                                d["v_scale_pages"], pg["kv_page_indptr"], pg["kv_last_page_len"],
+                                d["kv_page_indptr"], d["kv_last_page_len"], d["kv_page_indices"],
+                                f["scale"])
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 48, 64])
+def test_int4_paged_matches_oracle_and_ragged(cuda_device, page_size):
+    f = random_int4(make_small(4, 32, 8, 128, [1000, 1, 0, 2500], seed=page_size))
+    pg = to_paged_int4(f, page_size, seed=page_size + 1)
+    o, lse = _paged_call(pg, f, cuda_device)
+    o_r, lse_r = _run(f, cuda_device)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = _ref(f)
+    err = errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
+    assert_within(err, **TIGHT, what=f"paged int4 P={page_size}")
+    # the same keys through the ragged INT4 path: the same bits
+    assert torch.equal(o, o_r) and torch.equal(lse, lse_r)
+
+
+def test_int4_unused_page_rows_do_not_leak(cuda_device):
+    """Rows past a request's last key in its last page hold NaN scales and
+    arbitrary codes: the result is that of zeroed rows."""
+    f = random_int4(make_small(2, 16, 4, 128, [45, 70], seed=31))
+    pg = to_paged_int4(f, 32, seed=5, spare_pages=0)
+    o0, l0 = _paged_call(pg, f, cuda_device)
+    bad = dict(pg)
+    n, P = pg["k_pages_int4"].shape[:2]
+    used = torch.zeros(n, P, dtype=torch.bool)
+    ip, idx, last = pg["kv_page_indptr"], pg["kv_page_indices"], pg["kv_last_page_len"]
+    for b in range(len(ip) - 1):
+        for j in range(int(ip[b]), int(ip[b + 1])):
+            cnt = int(last[b]) if j == int(ip[b + 1]) - 1 else P
+            used[int(idx[j]), :cnt] = True
+    for name in ("k", "v"):
+        codes = pg[name + "_pages_int4"].clone()
+        codes[~used] = 0x88
+        bad[name + "_pages_int4"] = codes
+        sc = pg[name + "_scale_pages"].clone().reshape(-1, n, P)
+        sc[:, ~used] = float("nan")
+        bad[name + "_scale_pages"] = sc.reshape(-1, n * P).contiguous()
+    o1, l1 = _paged_call(bad, f, cuda_device)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o1).all() and torch.isfinite(l1).all()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def test_int4_rejects_misaligned_scales(cuda_device):
+    f = random_int4(make_small(1, 8, 2, 128, [100], seed=2))
+    dev = cuda_device
+    ks = torch.zeros(2 * 100 + 1, dtype=torch.float32, device=dev)[1:].view(2, 100)   # 4-byte aligned only
+    ks.copy_(f["k_scale_int4"].to(dev))
+    d = {k: f[k].to(dev) for k in ("q", "k_int4", "v_int4", "v_scale_int4")}
+    with pytest.raises(fd.FdError) as e:
+        fd.decode_int4(d["q"], d["k_int4"], d["v_int4"], ks, d["v_scale_int4"], f["kv_indptr"],
+                       f["kv_indptr"].to(dev), f["scale"])
+    assert e.value.code == -1

@@ -224,3 +224,66 @@ def to_fp8(inp: dict) -> dict:
         out[name + "_fp8"] = q.view(torch.uint8).contiguous()
         out[name + "_scale"] = scale.contiguous()
     return out
+
+
+def to_int4(inp: dict) -> dict:
+    """Quantise an input's K and V to packed INT4 (storage layout only).
+
+    Per tensor, key row t and KV head h: scale[h, t] = max |x[t, h, :]| / 7 in
+    fp32 (1 for an all-zero row); codes = round-half-even(x / scale) clamped to
+    -8..7, two per byte (element 2j in the low nibble of byte j, 2j + 1 in the
+    high nibble, two's complement).  Returns a copy of `inp` with k_int4,
+    v_int4 (uint8 [T, Hkv, D/2]) and k_scale_int4, v_scale_int4 (fp32
+    [Hkv, T], head-major).
+    """
+    out = dict(inp)
+    for name in ("k", "v"):
+        x = inp[name].float()
+        amax = x.abs().amax(dim=2) if x.shape[0] else torch.zeros(x.shape[:2])
+        scale = torch.where(amax > 0, amax / 7.0, torch.ones_like(amax)).float()   # [T, Hkv]
+        c = torch.round(x / scale[:, :, None]).clamp(-8, 7).to(torch.int16)
+        u = (c & 0xF).to(torch.uint8)
+        out[name + "_int4"] = (u[..., 0::2] | (u[..., 1::2] << 4)).contiguous()
+        out[name + "_scale_int4"] = scale.t().contiguous()
+    return out
+
+
+def random_int4(inp: dict, *, seed: int = 11) -> dict:
+    """Seeded uniformly random INT4 K/V for `inp`'s shapes: every byte (so
+    every code -8..7 in both nibbles) equally likely, scales drawn from
+    N(0, 0.5^2) (signs of both kinds).  Same keys as to_int4."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    out = dict(inp)
+    T, Hkv, D = inp["k"].shape
+    for name in ("k", "v"):
+        out[name + "_int4"] = torch.randint(0, 256, (T, Hkv, D // 2), generator=g,
+                                            dtype=torch.int32).to(torch.uint8)
+        out[name + "_scale_int4"] = (torch.randn((Hkv, T), generator=g) * 0.5).float()
+    return out
+
+
+def to_paged_int4(inp: dict, page_size: int, *, seed: int = 7, spare_pages: int = 3) -> dict:
+    """Lay an INT4 input (to_int4 / random_int4) out as a paged KV cache, with
+    the same page order as to_paged(inp, page_size, seed=seed, spare_pages=...).
+
+    Returns k_pages_int4 / v_pages_int4 [num_pages, page_size, Hkv, D/2]
+    (unused rows zero), k_scale_pages / v_scale_pages fp32 [Hkv, num_pages *
+    page_size] (entry h, p * page_size + r for row r of page p; unused zero),
+    and the page table of to_paged.
+    """
+    codes = to_paged(dict(inp, k=inp["k_int4"], v=inp["v_int4"]), page_size, seed=seed,
+                     spare_pages=spare_pages)
+    # scales as [T, Hkv, 1] rows, paged the same way
+    sc = to_paged(dict(inp, k=inp["k_scale_int4"].t()[:, :, None].contiguous(),
+                       v=inp["v_scale_int4"].t()[:, :, None].contiguous()),
+                  page_size, seed=seed, spare_pages=spare_pages)
+    out = dict(codes)
+    out["k"], out["v"] = inp["k"], inp["v"]
+    out["k_pages_int4"], out["v_pages_int4"] = codes["k_pages"], codes["v_pages"]
+    del out["k_pages"], out["v_pages"]
+    n = sc["k_pages"].shape[0]
+    Hkv = inp["k"].shape[1]
+    for name in ("k", "v"):
+        out[name + "_scale_pages"] = sc[name + "_pages"].reshape(n * page_size, Hkv).t().contiguous()
+    return out
