@@ -290,15 +290,15 @@ int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_
  * ragged, [num_pages, page_size, Hkv, D/2] paged.  Byte j of a row holds
  * element 2j in its low nibble and element 2j + 1 in its high nibble, each a
  * four-bit two's-complement code c in -8..7.  k_scale and v_scale (device,
- * fp32, 16-byte aligned) are head-major: [Hkv][rows], rows = T (ragged) or
+ * fp32) are head-major: [Hkv][rows], rows = T (ragged) or
  * num_pages * page_size (paged; entry h * rows + p * page_size + r belongs to
  * row r of page p).  The value of a K element is c * k_scale[h][row], and
  * likewise for V.  q stays bf16 and O, LSE fp32; the result is attention over
  * the dequantised K and V (the codes widen to bf16 exactly; each row's K scale
  * multiplies its logit and its V scale its softmax weight in P V, all in
- * fp32).  A scale of +-inf or NaN propagates.  Num_kv_heads * rows must stay
- * below 2^31 - 64, else FD_ERR_UNSUPPORTED.  Workspace and plan as for
- * fd_decode / fd_decode_paged.
+ * fp32).  A scale of +-inf or NaN propagates; the scales of rows past a
+ * request's last key (the rest of its last page) are never used.  Workspace
+ * and plan as for fd_decode / fd_decode_paged.
  */
 int fd_decode_int4(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                    const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,

@@ -132,6 +132,30 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), the bytes past
+// src_bytes (0 or 16) zero-filled, with an L2 eviction policy.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes,
+                                            uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+                 "l"(src), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared, zero-filled past src_bytes (0 or 4).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued before has
+// landed (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // 3-D tiled TMA load of box (x, y, z) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t x,
                                             int32_t y, int32_t z, uint32_t bar, uint64_t policy)

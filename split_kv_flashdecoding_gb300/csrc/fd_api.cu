@@ -92,43 +92,6 @@ int make_kv_map_fp8(CUtensorMap *map, const void *base, int64_t rows, int num_kv
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
 }
 
-// INT4 K or V [rows, Hkv, 64] (two four-bit codes per byte) as a 2-D tensor of
-// rows x Hkv*64 bytes; one box = box_rows rows x the head's 64 bytes, 64-byte
-// swizzle, zero fill past the last row.
-int make_kv_map_int4(CUtensorMap *map, const void *base, int64_t rows, int num_kv_heads, int box_rows)
-{
-    auto encode = tensor_map_encoder();
-    if (!encode)
-        return FD_ERR_CUDA;
-    const cuuint64_t dims[2] = {(cuuint64_t)num_kv_heads * kHeadDim / 2, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)num_kv_heads * kHeadDim / 2};
-    const cuuint32_t box[2] = {kHeadDim / 2, (cuuint32_t)box_rows};
-    const cuuint32_t elem_strides[2] = {1, 1};
-    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
-                              strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
-}
-
-// INT4 scales [Hkv][rows] fp32 as a 1-D tensor of Hkv*rows entries; one box =
-// `box` entries, zero fill past the end.
-int make_scale_map(CUtensorMap *map, const float *base, int64_t entries, int box)
-{
-    auto encode = tensor_map_encoder();
-    if (!encode)
-        return FD_ERR_CUDA;
-    const cuuint64_t dims[1] = {(cuuint64_t)entries};
-    const cuuint64_t strides[1] = {0};   // rank 1: no strides are read
-    const cuuint32_t boxdim[1] = {(cuuint32_t)box};
-    const cuuint32_t elem_strides[1] = {1};
-    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float *>(base),
-                              dims, strides, boxdim, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
-}
-
 int check_info(const fd_plan_info *info)
 {
     if (!info)
@@ -236,13 +199,12 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     if (!(scale == scale))
         return FD_ERR_INVALID_ARG;
     const int kv_type = quant ? quant->type : fd::kKvTypeBf16;
-    const bool int4 = kv_type == fd::kKvTypeInt4;
-    // INT4 scales are read by 16-byte TMA boxes; FP8 scales by plain loads
-    if (quant && (!quant->k_scale || !quant->v_scale || !aligned(quant->k_scale, int4 ? 16 : 4) ||
-                  !aligned(quant->v_scale, int4 ? 16 : 4)))
+    if (quant && (!quant->k_scale || !quant->v_scale || !aligned(quant->k_scale, 4) ||
+                  !aligned(quant->v_scale, 4)))
         return FD_ERR_INVALID_ARG;
 
     fd::KvMaps maps;
+    memset(&maps, 0, sizeof maps);   // INT4: loaded without tensor maps
     int rc;
     const int64_t rows = paged ? (int64_t)paged->num_pages * paged->page_size : info->total_tokens;
     const int box_rows = paged && paged->page_size % kBoxRows != 0 ? 16 : kBoxRows;
@@ -250,26 +212,10 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
         if ((rc = make_kv_map_fp8(&maps.k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
             (rc = make_kv_map_fp8(&maps.v, v, rows, info->num_kv_heads, box_rows)) != FD_OK)
             return rc;
-    } else if (int4) {
-        // the scale boxes start at element kvh * rows + row: a 32-bit coordinate
-        if ((int64_t)info->num_kv_heads * rows > INT32_MAX - 64)
-            return FD_ERR_UNSUPPORTED;
-        // ragged rows start anywhere: a box of 36 covers 32 scales from the
-        // 16-byte boundary at or below the first; page rows start on one
-        const int scale_box = paged ? box_rows : kBoxRows + 4;
-        const int64_t entries = (int64_t)info->num_kv_heads * rows;
-        if ((rc = make_kv_map_int4(&maps.k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
-            (rc = make_kv_map_int4(&maps.v, v, rows, info->num_kv_heads, box_rows)) != FD_OK ||
-            (rc = make_scale_map(&maps.ks, quant->k_scale, entries, scale_box)) != FD_OK ||
-            (rc = make_scale_map(&maps.vs, quant->v_scale, entries, scale_box)) != FD_OK)
+    } else if (kv_type == fd::kKvTypeBf16) {
+        if ((rc = make_kv_map(&maps.k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
+            (rc = make_kv_map(&maps.v, v, rows, info->num_kv_heads, box_rows)) != FD_OK)
             return rc;
-    } else if ((rc = make_kv_map(&maps.k, k, rows, info->num_kv_heads, box_rows)) != FD_OK ||
-               (rc = make_kv_map(&maps.v, v, rows, info->num_kv_heads, box_rows)) != FD_OK) {
-        return rc;
-    }
-    if (!int4) {
-        maps.ks = maps.k;
-        maps.vs = maps.v;
     }
 
     fd::SplitParams p;
@@ -311,6 +257,8 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
         memcpy(p.last_len_param, paged->last_len_host, (size_t)info->batch * sizeof(int32_t));
     p.kv_type = kv_type;
     p.kv_rows = (int32_t)rows;
+    p.k_data = static_cast<const uint8_t *>(k);
+    p.v_data = static_cast<const uint8_t *>(v);
     p.k_scale = quant ? quant->k_scale : nullptr;
     p.v_scale = quant ? quant->v_scale : nullptr;
     // Persistent grid: at most one wave of resident CTAs on the plan's SMs.

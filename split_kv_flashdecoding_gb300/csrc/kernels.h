@@ -56,10 +56,12 @@ struct SplitParams {
     // Element type of K/V (kKvTypeBf16, kKvTypeFp8, kKvTypeInt4), dequantised in
     // registers.  FP8 (E4M3): one byte per element; k_scale, v_scale [Hkv]
     // (device) multiply the head's K and V values.  INT4: two four-bit codes
-    // per byte, and one scale per key row and head, read through the scale
-    // tensor maps ([Hkv][kv_rows] fp32).
+    // per byte, and one scale per key row and head (k_scale, v_scale
+    // [Hkv][kv_rows] fp32), loaded without tensor maps from k_data / v_data.
     int32_t kv_type;
     int32_t kv_rows;            // rows of K/V: T keys, or num_pages * page_size
+    const uint8_t *k_data;      // K and V themselves
+    const uint8_t *v_data;
     const float *k_scale;
     const float *v_scale;
 };
@@ -68,10 +70,9 @@ constexpr int kKvTypeBf16 = 0;
 constexpr int kKvTypeFp8 = 1;
 constexpr int kKvTypeInt4 = 2;
 
-// The split kernel's TMA descriptors: K and V, and (INT4) the K and V scales;
-// for the other types ks / vs repeat k / v and are not read.
+// The split kernel's TMA descriptors of K and V (INT4 K/V: not read).
 struct KvMaps {
-    CUtensorMap k, v, ks, vs;
+    CUtensorMap k, v;
 };
 
 struct MergeParams {

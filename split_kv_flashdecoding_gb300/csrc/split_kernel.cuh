@@ -75,33 +75,40 @@ enum KvType { kKvBf16 = 0, kKvFp8 = 1, kKvInt4 = 2 };
 //    values), 16-byte chunks XOR-swizzled by r % 8; a second 16-row page box
 //    lands 16 rows further.
 //  INT4: a tensor is [32 rows][64 bytes] (128 four-bit values), 16-byte chunks
-//    XOR-swizzled by (r / 2) % 4 (the 64-byte swizzle), then the rows' K scales
-//    and V scales (fp32), each in a 256-byte slot: one box of kScaleBox scales
-//    per 32 rows (ragged: from the 16-byte boundary at or below the tile's
-//    first scale, so the tile's scales start srem = 0..3 entries in), or for
-//    16-row pages two boxes of 16, the second 128 bytes in (kScaleGap bytes
-//    after the first box's end).  Every copy lands on a 128-byte boundary, and
-//    the stage stride is a multiple of 512 bytes, the swizzle's period.
+//    XOR-swizzled by (r / 2) % 4, then the rows' K scales and V scales (fp32,
+//    32 each).  INT4 stages are filled by the producer lanes' cp.async copies
+//    (kDirect): with 64-byte rows and per-row scales, TMA boxes cost more
+//    producer and copy-engine time per byte than the copies do.
 template <int KV, int DT>
 struct Stage {
     static constexpr bool kFp8 = DT == kKvFp8;
     static constexpr bool kInt4 = DT == kKvInt4;
-    static constexpr int kTensorBytes = kInt4 ? kTile * 64 : kFp8 ? kTile * 128 : 2 * kHalfBytes;
+    static constexpr bool kDirect = kInt4;
+    static constexpr int kRowBytes = kInt4 ? kHeadDim / 2 : kFp8 ? kHeadDim : 2 * kHeadDim;
+    static constexpr int kFullArrivals = kDirect ? 32 : 1;   // full barrier: arrivals per phase
+    static constexpr int kTensorBytes = kTile * kRowBytes;
     static constexpr int kBoxRows = KV == kKvPaged16 ? 16 : kTile;
-    static constexpr int kScaleBox = KV == kKvRagged ? kTile + 4 : kBoxRows;   // fp32 entries
-    static constexpr int kKsOff = 2 * kTensorBytes;
-    static constexpr int kVsOff = kKsOff + 256;
-    static constexpr int kScaleGap = KV == kKvPaged16 ? 128 - 16 * 4 : 0;
-    static constexpr int kScaleTx = kInt4 ? 2 * (kTile / kBoxRows) * kScaleBox * 4 : 0;
-    static constexpr int kTxBytes = 2 * kTensorBytes + kScaleTx;   // bytes one stage's copies bring
-    static constexpr int kBytes = kInt4 ? (kVsOff + 256 + 511) / 512 * 512 : 2 * kTensorBytes;
-    // a tensor copy's shared-memory destination must be 128-byte aligned
-    static_assert(kTensorBytes % 512 == 0 && kKsOff % 128 == 0 && kVsOff % 128 == 0 &&
-                      kBytes % 512 == 0, "stage copies on 128-byte boundaries");
-    static_assert(!kInt4 || (kBoxRows == kTile ? kScaleBox * 4 : 128 + kScaleBox * 4) <= 256,
-                  "the scale boxes fit their 256-byte slot");
+    static constexpr int kKsOff = 2 * kTensorBytes;            // INT4 scales
+    static constexpr int kVsOff = kKsOff + kTile * 4;
+    static constexpr int kBytes = kInt4 ? kVsOff + kTile * 4 : 2 * kTensorBytes;
     static constexpr int kHalfStride = KV == kKvPaged16 ? 2048 : kHalfBytes;
     static constexpr int kBlockStride = KV == kKvPaged16 ? 4096 : 2048;
+    // a TMA copy's shared-memory destination must be 128-byte aligned
+    static_assert(kDirect || kTensorBytes % 1024 == 0, "stage copies on 128-byte boundaries");
+
+    // Offset in a tensor's part of the stage of 16-byte chunk c of key row r
+    // (the bf16 and FP8 layouts are those of the TMA boxes' 128-byte swizzle,
+    // which XORs the chunk index with address bits 7-9).
+    static __device__ __forceinline__ uint32_t chunk_offset(int r, int c)
+    {
+        if constexpr (kInt4)
+            return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+        else if constexpr (kFp8)
+            return r * 128 + ((c ^ (r & 7)) << 4);
+        else
+            return (c >> 3) * kHalfStride + (r >> 4) * kBlockStride + (r & 15) * 128 +
+                   (((c & 7) ^ (r & 7)) << 4);
+    }
 };
 constexpr int kMaxGroup = 8;                   // rows 8-15 of the MMA carry the lo part of P
 
@@ -111,22 +118,20 @@ enum Misc { kAbort, kIssued, kDescs, kLast, kFinalK, kMiscCount };
 // warps: request, its split prefix and count, split, key range [t0, t1)
 // relative to the request's first key, KV head, index of the item's first
 // tile in the CTA's stream of tiles, the head's K and V scales (FP8 K/V; float
-// bits), where the tiles' scales start in their stage (INT4 K/V: srem), and a
-// state: kItemOk, kItemBad (outside the plan: the CTA stops) or kItemEnd (no
-// further item; the previous one was the CTA's last).
-enum Desc { kDB, kDPrefix, kDSplits, kDS, kDT0, kDT1, kDKvh, kDGt0, kDState, kDKs, kDVs, kDSrem,
-            kDescInts };
+// bits), and a state: kItemOk, kItemBad (outside the plan: the CTA stops) or
+// kItemEnd (no further item; the previous one was the CTA's last).
+enum Desc { kDB, kDPrefix, kDSplits, kDS, kDT0, kDT1, kDKvh, kDGt0, kDState, kDKs, kDVs, kDescInts };
 enum ItemState { kItemBad = 0, kItemOk = 1, kItemEnd = 2 };
 constexpr int kDescSlots = 4;
 
 struct Item {
-    int32_t b, prefix, splits, s, t0, t1, kvh, gt0, state, ks, vs, srem;
+    int32_t b, prefix, splits, s, t0, t1, kvh, gt0, state, ks, vs;
 };
 
 __device__ __forceinline__ Item read_item(const volatile int *d)
 {
     return Item{d[kDB], d[kDPrefix], d[kDSplits], d[kDS], d[kDT0], d[kDT1],
-                d[kDKvh], d[kDGt0], d[kDState], d[kDKs], d[kDVs], d[kDSrem]};
+                d[kDKvh], d[kDGt0], d[kDState], d[kDKs], d[kDVs]};
 }
 
 // Shared memory of the one-item kernel: [stage ring | full[NS] empty[NS] |
@@ -420,12 +425,11 @@ __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, in
 //    multiplies its logit, and its V scale its probability in P V (the row sum
 //    takes the probability alone).  ldmatrix.trans of V gives lane (g, t4) dims
 //    32c + 4g .. +3 of keys 2t4 and 2t4 + 1, so o_acc[4c + j] holds dims
-//    32c + 8t4 + j (and + 4).  The tile's scales start srem entries into the
-//    stage's scale boxes.
+//    32c + 8t4 + j (and + 4).
 template <int KV, int DT>
 __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uint32_t (&qa)[8][2],
                                              float qk_scale, int lane, float &m_run, float &l_part,
-                                             float (&o_acc)[16][4], int srem = 0)
+                                             float (&o_acc)[16][4])
 {
     using S = Stage<KV, DT>;
     const int t4 = lane & 3;
@@ -489,16 +493,15 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
     // ---- online softmax on row g_row (this thread's 8 scores of the tile)
     float x[8];
     float mt = -INFINITY;
-    const uint32_t ks_base = st + S::kKsOff + 4 * srem, vs_base = st + S::kVsOff + 4 * srem;
+    const uint32_t ks_base = st + S::kKsOff, vs_base = st + S::kVsOff;
 #pragma unroll
     for (int jn = 0; jn < 4; ++jn)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int key = 8 * jn + 2 * t4 + e;
             float logit = sc[jn][e] * qk_scale;
-            if constexpr (S::kInt4)   // keys 16..31 sit kScaleGap further (16-row pages)
-                logit = sc[jn][e] * lds_f32(ks_base + 4 * key + (jn >= 2 ? S::kScaleGap : 0)) *
-                        qk_scale;
+            if constexpr (S::kInt4)
+                logit = sc[jn][e] * lds_f32(ks_base + 4 * key) * qk_scale;
             const float v = key < n_valid ? logit : -INFINITY;
             x[2 * jn + e] = v;
             mt = fmaxf(mt, v);
@@ -535,7 +538,7 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
             // keys 16ks + 2t4 (+1) and 16ks + 8 + 2t4 (+1); a masked key's
             // scale (another request's row, or past the end) is not read
             const int k0 = 16 * ks + 2 * t4;
-            const uint32_t vk = vs_base + 4 * k0 + ks * S::kScaleGap;
+            const uint32_t vk = vs_base + 4 * k0;
             p0 = k0 < n_valid ? p0 * lds_f32(vk) : 0.f;
             p1 = k0 + 1 < n_valid ? p1 * lds_f32(vk + 4) : 0.f;
             p2 = k0 + 8 < n_valid ? p2 * lds_f32(vk + 32) : 0.f;
@@ -636,7 +639,6 @@ struct TileSource {
     static constexpr bool kPaged = KV != kKvRagged;
     const SplitParams &p;
     const CUtensorMap *tm_k, *tm_v;
-    const CUtensorMap *tm_ks, *tm_vs;   // INT4: the K and V scales
     uint8_t *ring;
     uint64_t *full;   // full[NS]
     uint64_t pol;
@@ -651,11 +653,9 @@ struct TileSource {
     int32_t cur_pg = 0, cur_off = 0;
 
     __device__ __forceinline__ TileSource(const SplitParams &p_, const CUtensorMap *k,
-                                          const CUtensorMap *v, const CUtensorMap *ks,
-                                          const CUtensorMap *vs, uint8_t *ring_, uint64_t *full_,
+                                          const CUtensorMap *v, uint8_t *ring_, uint64_t *full_,
                                           int lane_)
-        : p(p_), tm_k(k), tm_v(v), tm_ks(ks), tm_vs(vs), ring(ring_), full(full_),
-          pol(l2_evict_first_policy()), lane(lane_)
+        : p(p_), tm_k(k), tm_v(v), ring(ring_), full(full_), pol(l2_evict_first_policy()), lane(lane_)
     {
     }
 
@@ -724,43 +724,56 @@ struct TileSource {
         }
     }
 
-    // Put stream tile g (KV head kvh) into stage g % NS, per tensor and per box
-    // of rows: bf16, one 3-D box of both 64-column halves; FP8, one 2-D box of
-    // the rows' 128 bytes; INT4, one 2-D box of the rows' 64 bytes and a 1-D
-    // box of their scales (from the 16-byte boundary at or below the first).
+    // Put stream tile g (KV head kvh) into stage g % NS.
+    //  TMA (lane 0): per tensor and per box of rows -- bf16, one 3-D box of
+    //    both 64-column halves; FP8, one 2-D box of the rows' 128 bytes.
+    //  cp.async (INT4, every lane): the lane's share of the 16-byte chunks of
+    //    both tensors (rows past the end of K/V zero-filled) and the K and V
+    //    scale of row `lane`, then one arrival once its copies have landed.
     __device__ __forceinline__ void issue(int g, int kvh, int32_t ya, int32_t yb) const
     {
         const int s = g % NS;
         const uint32_t bar = smem_addr(&full[s]);
         const uint32_t dst = smem_addr(ring + s * SL::kBytes);
-        mbar_arrive_expect_tx(bar, SL::kTxBytes);
-        if constexpr (SL::kInt4) {
-            const int32_t x = kvh * (kHeadDim / 2);
-            const int32_t head_rows = kvh * p.kv_rows;   // the head's first scale
-            tma_load_2d(dst, tm_k, x, ya, bar, pol);
-            tma_load_2d(dst + SL::kTensorBytes, tm_v, x, ya, bar, pol);
-            tma_load_1d(dst + SL::kKsOff, tm_ks, (head_rows + ya) & ~3, bar, pol);
-            tma_load_1d(dst + SL::kVsOff, tm_vs, (head_rows + ya) & ~3, bar, pol);
-            if constexpr (SL::kBoxRows < kTile) {
-                tma_load_2d(dst + 16 * 64, tm_k, x, yb, bar, pol);
-                tma_load_2d(dst + SL::kTensorBytes + 16 * 64, tm_v, x, yb, bar, pol);
-                tma_load_1d(dst + SL::kKsOff + 128, tm_ks, (head_rows + yb) & ~3, bar, pol);
-                tma_load_1d(dst + SL::kVsOff + 128, tm_vs, (head_rows + yb) & ~3, bar, pol);
+        if constexpr (SL::kDirect) {
+            constexpr int kChunks = SL::kRowBytes / 16;   // per key row
+            const int64_t row_stride = (int64_t)p.num_kv_heads * SL::kRowBytes;
+            const uint8_t *kb = p.k_data + kvh * SL::kRowBytes;
+            const uint8_t *vb = p.v_data + kvh * SL::kRowBytes;
+#pragma unroll
+            for (int i = 0; i < kChunks; ++i) {
+                const int idx = lane + 32 * i, r = idx / kChunks, c = idx % kChunks;
+                const int32_t row = SL::kBoxRows == kTile || r < 16 ? ya + r : yb + (r - 16);
+                const bool in = row < p.kv_rows;
+                const int64_t off = (int64_t)(in ? row : 0) * row_stride + c * 16;
+                const uint32_t so = SL::chunk_offset(r, c);
+                cp_async_16(dst + so, kb + off, in ? 16 : 0, pol);
+                cp_async_16(dst + SL::kTensorBytes + so, vb + off, in ? 16 : 0, pol);
             }
-        } else if constexpr (SL::kFp8) {
-            const int32_t x = kvh * kHeadDim;
-            tma_load_2d(dst, tm_k, x, ya, bar, pol);
-            tma_load_2d(dst + SL::kTensorBytes, tm_v, x, ya, bar, pol);
-            if constexpr (SL::kBoxRows < kTile) {
-                tma_load_2d(dst + 16 * 128, tm_k, x, yb, bar, pol);
-                tma_load_2d(dst + SL::kTensorBytes + 16 * 128, tm_v, x, yb, bar, pol);
-            }
+            const int32_t row = SL::kBoxRows == kTile || lane < 16 ? ya + lane : yb + (lane - 16);
+            const bool in = row < p.kv_rows;
+            const int64_t si = (int64_t)kvh * p.kv_rows + (in ? row : 0);
+            cp_async_4(dst + SL::kKsOff + 4 * lane, p.k_scale + si, in ? 4 : 0);
+            cp_async_4(dst + SL::kVsOff + 4 * lane, p.v_scale + si, in ? 4 : 0);
+            cp_async_mbar_arrive(bar);
         } else {
-            tma_load_3d(dst, tm_k, 0, ya, 2 * kvh, bar, pol);
-            tma_load_3d(dst + SL::kTensorBytes, tm_v, 0, ya, 2 * kvh, bar, pol);
-            if constexpr (SL::kBoxRows < kTile) {
-                tma_load_3d(dst + SL::kBlockStride, tm_k, 0, yb, 2 * kvh, bar, pol);
-                tma_load_3d(dst + SL::kTensorBytes + SL::kBlockStride, tm_v, 0, yb, 2 * kvh, bar, pol);
+            mbar_arrive_expect_tx(bar, SL::kBytes);
+            if constexpr (SL::kFp8) {
+                const int32_t x = kvh * kHeadDim;
+                tma_load_2d(dst, tm_k, x, ya, bar, pol);
+                tma_load_2d(dst + SL::kTensorBytes, tm_v, x, ya, bar, pol);
+                if constexpr (SL::kBoxRows < kTile) {
+                    tma_load_2d(dst + 16 * 128, tm_k, x, yb, bar, pol);
+                    tma_load_2d(dst + SL::kTensorBytes + 16 * 128, tm_v, x, yb, bar, pol);
+                }
+            } else {
+                tma_load_3d(dst, tm_k, 0, ya, 2 * kvh, bar, pol);
+                tma_load_3d(dst + SL::kTensorBytes, tm_v, 0, ya, 2 * kvh, bar, pol);
+                if constexpr (SL::kBoxRows < kTile) {
+                    tma_load_3d(dst + SL::kBlockStride, tm_k, 0, yb, 2 * kvh, bar, pol);
+                    tma_load_3d(dst + SL::kTensorBytes + SL::kBlockStride, tm_v, 0, yb, 2 * kvh, bar,
+                                pol);
+                }
             }
         }
     }
@@ -788,9 +801,8 @@ __device__ __forceinline__ bool item_range(const SplitParams &p, const SplitCoor
 
 __device__ __forceinline__ void write_desc(volatile int *d, const SplitCoord &c, int32_t t0,
                                            int32_t t1, int kvh, int gt0, int state, float ks = 1.f,
-                                           float vs = 1.f, int srem = 0)
+                                           float vs = 1.f)
 {
-    d[kDSrem] = srem;
     d[kDKs] = __float_as_int(ks);
     d[kDVs] = __float_as_int(vs);
     d[kDB] = c.b;
@@ -802,19 +814,6 @@ __device__ __forceinline__ void write_desc(volatile int *d, const SplitCoord &c,
     d[kDKvh] = kvh;
     d[kDGt0] = gt0;
     d[kDState] = state;
-}
-
-// INT4 K/V: where an item's tile scales start in their stage.  A ragged item's
-// tiles start at key rows base + t0 + 32i, so their scales (head kvh's entries
-// at kvh * kv_rows + row) all sit (kvh * kv_rows + base + t0) % 4 entries past
-// a 16-byte boundary; page rows start on one (page_size and kv_rows are
-// multiples of 16).
-template <int KV, int DT>
-__device__ __forceinline__ int scale_rem(const SplitParams &p, int kvh, int32_t base, int32_t t0)
-{
-    if constexpr (DT == kKvInt4 && KV == kKvRagged)
-        return (kvh * p.kv_rows + base + t0) & 3;
-    return 0;
 }
 
 __device__ __forceinline__ KeyIndex key_index(const SplitParams &p, bool paged)
@@ -1040,13 +1039,12 @@ template <int G, int NC, int NS, int MIN_CTAS, int KV, int DT>
 __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     split_kv_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_ks,
-                    const __grid_constant__ CUtensorMap tm_vs,
                     const __grid_constant__ SplitParams p)
 {
     using SG = Stage<KV, DT>;
     using L = SingleLayout<G, NC, NS, SG::kBytes>;
     constexpr bool paged = KV != kKvRagged;
+    constexpr bool warp_loop = paged || SG::kDirect;   // the whole producer warp runs the issue loop
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1087,13 +1085,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         // past the batch's items have nothing to do
         const bool none = !found && p.device_plan;
         if (lane == 0) {
-            write_desc(desc, c, t0, t1, kvh, 0, ok ? kItemOk : (none ? kItemEnd : kItemBad), 1.f,
-                       1.f, scale_rem<KV, DT>(p, kvh, c.base, t0));
+            write_desc(desc, c, t0, t1, kvh, 0, ok ? kItemOk : (none ? kItemEnd : kItemBad));
             misc[kAbort] = ok || none ? 0 : 1;
             misc[kIssued] = 0;
             misc[kLast] = 0;
             for (int s = 0; s < NS; ++s) {
-                mbar_init(smem_addr(&bars[s]), 1);        // full: producer arrive + TMA bytes
+                mbar_init(smem_addr(&bars[s]), SG::kFullArrivals);   // full: producer arrive(s) + bytes
                 mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: the stage's consumer warp
             }
             fence_mbar_init();
@@ -1101,22 +1098,22 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                 report(p.status, FD_ERR_DEVICE_BOUNDS);
         }
         __syncwarp();
-        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, &tm_ks, &tm_vs, smem, bars, lane);
+        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
         const int n_tiles = ok ? (t1 - t0 + kTile - 1) / kTile : 0;
         const int first = min(NS, n_tiles);
-        if (ok && (paged || lane == 0)) {
+        if (ok && (warp_loop || lane == 0)) {
             src.begin_item(t0, c.base, c.pages);
             for (int i = 0; i < first; ++i) {
                 int32_t ya = 0, yb = 0;
                 src.tile_rows(i, ya, yb);
-                if (lane == 0)
+                if (SG::kDirect || lane == 0)
                     src.issue(i, kvh, ya, yb);
             }
         }
         if (lane == 0)
             misc[kIssued] = first;
         __syncthreads();   // the barriers are initialised
-        if (ok && (paged || lane == 0)) {
+        if (ok && (warp_loop || lane == 0)) {
             int issued = first;
             for (int i = first; i < n_tiles; ++i) {
                 int32_t ya = 0, yb = 0;
@@ -1130,13 +1127,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                     } else if (misc[kAbort]) {
                         go = 0;
                     }
-                    if (go)
+                    if (go && !SG::kDirect)
                         src.issue(i, kvh, ya, yb);
                 }
-                if constexpr (paged)
+                if constexpr (warp_loop)
                     go = __shfl_sync(0xffffffffu, go, 0);
                 if (!go)
                     break;
+                if constexpr (SG::kDirect)
+                    src.issue(i, kvh, ya, yb);
                 issued = i + 1;
             }
             if (lane == 0)
@@ -1166,7 +1165,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                     break;
                 }
                 consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc, it.srem);
+                                     qk, lane, m_run, l_part, o_acc);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1213,13 +1212,12 @@ template <int G, int NC, int NS, int MIN_CTAS, int KV, int DT>
 __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
     split_kv_persistent_kernel(const __grid_constant__ CUtensorMap tm_k,
                                const __grid_constant__ CUtensorMap tm_v,
-                               const __grid_constant__ CUtensorMap tm_ks,
-                               const __grid_constant__ CUtensorMap tm_vs,
                                const __grid_constant__ SplitParams p)
 {
     using SG = Stage<KV, DT>;
     using L = PersistentLayout<G, NC, NS, SG::kBytes>;
     constexpr bool paged = KV != kKvRagged;
+    constexpr bool warp_loop = paged || SG::kDirect;   // the whole producer warp runs the issue loop
     constexpr int kProducer = NC;   // the epilogue warp is NC + 1
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1253,7 +1251,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
             misc[kLast] = 0;
             misc[kFinalK] = -1;   // set to the last item's index; stays -1 for no items
             for (int s = 0; s < NS; ++s) {
-                mbar_init(smem_addr(&bars[s]), 1);        // full: producer arrive + TMA bytes
+                mbar_init(smem_addr(&bars[s]), SG::kFullArrivals);   // full: producer arrive(s) + bytes
                 mbar_init(smem_addr(&bars[NS + s]), 1);   // empty: the stage's consumer warp
             }
             for (int s = 0; s < kDescSlots; ++s) {
@@ -1277,7 +1275,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
         const KeyIndex ki = key_index(p, paged);
         SplitCursor cursor;
         cursor.empty_split = p.device_plan;
-        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, &tm_ks, &tm_vs, smem, bars, lane);
+        TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
         int gt = 0;      // tiles issued so far (index of the stream's next tile)
         int descs = 0;   // descriptors published (lane 0)
 
@@ -1285,7 +1283,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
         // the CTA stops (a wait ran out, or another warp gave up).
         auto issue_range = [&](int i0, int i1, int kvh) -> bool {
             int stop = 0;
-            if (paged || lane == 0) {
+            if (warp_loop || lane == 0) {
                 for (int i = i0; i < i1; ++i) {
                     int32_t ya = 0, yb = 0;
                     src.tile_rows(i, ya, yb);
@@ -1300,15 +1298,17 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                         } else if (misc[kAbort]) {
                             go = 0;
                         }
-                        if (go)
+                        if (go && !SG::kDirect)
                             src.issue(gt, kvh, ya, yb);
                     }
-                    if constexpr (paged)
+                    if constexpr (warp_loop)
                         go = __shfl_sync(0xffffffffu, go, 0);
                     if (!go) {
                         stop = 1;
                         break;
                     }
+                    if constexpr (SG::kDirect)
+                        src.issue(gt, kvh, ya, yb);
                     ++gt;
                 }
             }
@@ -1382,7 +1382,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                         vs = __ldg(p.v_scale + kvh);
                     }
                     write_desc(desc + slot * kDescInts, c, t0, t1, kvh, gt, ok ? kItemOk : kItemBad,
-                               ks, vs, scale_rem<KV, DT>(p, kvh, c.base, t0));
+                               ks, vs);
                     ++descs;
                     const uint32_t fb = smem_addr(&item_full[slot]);
                     if (ok) {
@@ -1453,7 +1453,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                     break;
                 }
                 consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc, it.srem);
+                                     qk, lane, m_run, l_part, o_acc);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1600,7 +1600,7 @@ cudaError_t launch_kernel(Kernel kern, bool (&configured)[64], int smem_bytes, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, m.k, m.v, m.ks, m.vs, p);
+    return cudaLaunchKernelEx(&cfg, kern, m.k, m.v, p);
 }
 
 // Stages in the ring: FP8 and INT4 tiles are half the bytes or less, so the

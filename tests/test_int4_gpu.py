@@ -136,12 +136,20 @@ def test_int4_unused_page_rows_do_not_leak(cuda_device):
 
 
 def test_int4_rejects_misaligned_scales(cuda_device):
+    """A scale pointer that is not fp32-aligned is refused before any launch."""
+    import ctypes
     f = random_int4(make_small(1, 8, 2, 128, [100], seed=2))
     dev = cuda_device
-    ks = torch.zeros(2 * 100 + 1, dtype=torch.float32, device=dev)[1:].view(2, 100)   # 4-byte aligned only
-    ks.copy_(f["k_scale_int4"].to(dev))
-    d = {k: f[k].to(dev) for k in ("q", "k_int4", "v_int4", "v_scale_int4")}
-    with pytest.raises(fd.FdError) as e:
-        fd.decode_int4(d["q"], d["k_int4"], d["v_int4"], ks, d["v_scale_int4"], f["kv_indptr"],
-                       f["kv_indptr"].to(dev), f["scale"])
-    assert e.value.code == -1
+    d = {k: f[k].to(dev) for k in ("q", "k_int4", "v_int4", "k_scale_int4", "v_scale_int4")}
+    ip = np.ascontiguousarray(f["kv_indptr"].numpy().astype(np.int32))
+    ipd = f["kv_indptr"].to(dev)
+    o = torch.empty((1, 8, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((1, 8), dtype=torch.float32, device=dev)
+    ws = torch.zeros(fd.workspace_bytes(1, 8, 2, 128, f["kv_indptr"]), dtype=torch.uint8, device=dev)
+    P = ctypes.c_void_p
+    rc = fd.lib().fd_decode_int4(1, 8, 2, 128, ip.ctypes.data_as(P), P(ipd.data_ptr()),
+                                 P(d["q"].data_ptr()), P(d["k_int4"].data_ptr()),
+                                 P(d["v_int4"].data_ptr()), P(d["k_scale_int4"].data_ptr() + 2),
+                                 P(d["v_scale_int4"].data_ptr()), float(f["scale"]), P(o.data_ptr()),
+                                 P(lse.data_ptr()), P(ws.data_ptr()), ws.numel(), None)
+    assert rc == -1
