@@ -277,6 +277,19 @@ __device__ __forceinline__ void int4x8_to_bf16x2x4(uint32_t x, uint32_t (&r)[4])
     }
 }
 
+// 16 zero bytes to shared memory (32-bit shared address, 16-byte aligned).
+__device__ __forceinline__ void sts_zero16(uint32_t addr)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // One fp32 from shared memory (32-bit shared address).
 __device__ __forceinline__ float lds_f32(uint32_t addr)
 {
@@ -436,6 +449,23 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
     // ldmatrix: lane supplies row lr of matrix lm.  The 128-byte swizzle XORs
     // the 16-byte chunk index with the row index mod 8, which is lr here.
     const int lr = lane & 7, lm = lane >> 3;
+
+    // ---- rows past the last key (the rest of a page, another request's keys)
+    // get P = 0, but 0 * NaN would still reach O: a tile that ends early has
+    // its V rows from n_valid on zeroed (the stage is this warp's alone).  The
+    // proxy fence orders these writes before the stage's next TMA refill.
+    // INT4 needs none: its codes are finite, and a masked key's V scale is
+    // replaced by 0 before P V.
+    if constexpr (!S::kInt4) {
+        if (n_valid < kTile) {
+            constexpr int kChunks = S::kRowBytes / 16;
+            const uint32_t vt = st + S::kTensorBytes;
+            for (int idx = lane; idx < (kTile - n_valid) * kChunks; idx += 32)
+                sts_zero16(vt + S::chunk_offset(n_valid + idx / kChunks, idx % kChunks));
+            fence_proxy_async_shared();
+            __syncwarp();
+        }
+    }
 
     // ---- S = Q K^T : 4 key groups (n-tiles) of 8, 8 k-steps of 16 dims
     float sc[4][4];

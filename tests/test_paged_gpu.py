@@ -90,3 +90,53 @@ def test_page_index_outside_pool_is_flagged(cuda_device):
     o, lse = _decode_paged(pg, d, ws)
     assert fd.get_device_status(ws) == -6
     assert torch.isfinite(o).all()
+
+
+def _unused_rows(pg):
+    """[num_pages, page_size] mask of the pool rows no request's key occupies."""
+    n, P = pg["k_pages"].shape[:2]
+    used = torch.zeros(n, P, dtype=torch.bool)
+    ip, idx, last = pg["kv_page_indptr"], pg["kv_page_indices"], pg["kv_last_page_len"]
+    for b in range(len(ip) - 1):
+        for j in range(int(ip[b]), int(ip[b + 1])):
+            used[int(idx[j]), : int(last[b]) if j == int(ip[b + 1]) - 1 else P] = True
+    return ~used
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_nan_in_unused_page_rows_does_not_leak(cuda_device, page_size):
+    """The rows past a request's last key in its last page are read with the
+    page but must not touch the result: filled with NaN, they leave O and LSE
+    bit-identical to zero-filled ones (bf16 and FP8 pools)."""
+    from workloads import to_fp8
+    inp = make_small(3, 16, 4, 128, [45, 70, 129], seed=page_size)
+    pg = to_paged(inp, page_size, seed=5, spare_pages=0)
+    unused = _unused_rows(pg)
+    bad = dict(pg)
+    for name in ("k_pages", "v_pages"):
+        t = pg[name].clone()
+        t[unused] = float("nan")
+        bad[name] = t
+    o0, l0 = _decode_paged(pg, _paged_dev(pg, cuda_device))
+    o1, l1 = _decode_paged(bad, _paged_dev(bad, cuda_device))
+    torch.cuda.synchronize()
+    assert torch.isfinite(o1).all() and torch.isfinite(l1).all()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    # FP8: byte 0x7F is E4M3 NaN
+    f = to_fp8(inp)
+    pf = to_paged({**f, "k": f["k_fp8"], "v": f["v_fp8"]}, page_size, seed=5, spare_pages=0)
+    dev = cuda_device
+    ks, vs = f["k_scale"].to(dev), f["v_scale"].to(dev)
+    outs = []
+    for nan in (False, True):
+        kp, vp = pf["k_pages"].clone(), pf["v_pages"].clone()
+        if nan:
+            kp[unused] = 0x7F
+            vp[unused] = 0x7F
+        d = {k: pf[k].to(dev) for k in ("q", "kv_page_indptr", "kv_page_indices", "kv_last_page_len")}
+        outs.append(fd.decode_paged_fp8(d["q"], kp.to(dev), vp.to(dev), ks, vs, pf["kv_page_indptr"],
+                                        pf["kv_last_page_len"], d["kv_page_indptr"],
+                                        d["kv_last_page_len"], d["kv_page_indices"], f["scale"]))
+    torch.cuda.synchronize()
+    assert torch.isfinite(outs[1][0]).all() and torch.isfinite(outs[1][1]).all()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
