@@ -120,18 +120,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// 1-D tiled TMA load of the box starting at element x (x * element size a
-// multiple of 16 bytes) into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap *map, int32_t x,
-                                            uint32_t bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2}], [%3], %4;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 // 16-byte asynchronous copy global -> shared (L2 only), the bytes past
 // src_bytes (0 or 16) zero-filled, with an L2 eviction policy.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes,
