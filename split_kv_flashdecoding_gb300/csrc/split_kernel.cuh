@@ -1641,20 +1641,28 @@ constexpr int stages_for()
     return DT == kKvBf16 ? kNS : 2 * kNS;
 }
 
+// Consumer warps (and stages, two per warp) of the one-item kernel for INT4
+// K/V: its consumers are the bound (codes widened in registers), and a fifth
+// consumer warp still fits the register file at two CTAs per SM (12 warps x
+// 168 registers).  Measured: 64k step -2 %, 128k -4.5 %; FP8 was slower with 5.
+constexpr int kNCInt4 = 5;
+
 // One wave of items: one item per CTA.  More: the persistent kernel on
 // num_ctas CTAs.
 template <int G, int KV, int DT>
 cudaError_t launch_g(const KvMaps &m, const SplitParams &p, int num_ctas, cudaStream_t stream)
 {
     constexpr int NS = stages_for<DT>();
+    constexpr int NC1 = DT == kKvInt4 ? kNCInt4 : kNC;           // one-item kernel
+    constexpr int NS1 = DT == kKvInt4 ? 2 * kNCInt4 : NS;
     using SG = Stage<KV, DT>;
-    using LS = SingleLayout<G, kNC, NS, SG::kBytes>;
+    using LS = SingleLayout<G, NC1, NS1, SG::kBytes>;
     using LP = PersistentLayout<G, kNC, NS, SG::kBytes>;
     static_assert(kMinCtas * (LS::kAlloc + 1024) <= 233472 && kMinCtas * (LP::kAlloc + 1024) <= 233472,
                   "the resident CTAs must fit in shared memory");
     if (num_ctas >= p.num_work) {   // one wave: one item (or, device-side plan, at most one) per CTA
         static bool configured[64] = {};
-        return launch_kernel(split_kv_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured, LS::kAlloc,
+        return launch_kernel(split_kv_kernel<G, NC1, NS1, kMinCtas, KV, DT>, configured, LS::kAlloc,
                              LS::kWarps * 32, p.num_work, m, p, stream);
     }
     static bool configured[64] = {};
