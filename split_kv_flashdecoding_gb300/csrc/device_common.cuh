@@ -104,11 +104,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
-__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
-{
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
 // 2-D tiled TMA load of box (x, y) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t x,
                                             int32_t y, uint32_t bar, uint64_t policy)
@@ -188,22 +183,6 @@ __device__ __forceinline__ void griddep_wait()
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
 {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-__device__ __forceinline__ float warp_max(float x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
-}
-
-__device__ __forceinline__ float warp_sum(float x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
 }
 
 // ------------------------------------------------------- split derivation
