@@ -139,6 +139,26 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Prefetch a tiled TMA box into L2.  A hint: it changes no value, so it may
+// run before the wait for a preceding grid that writes the same memory (L2 is
+// where global memory is coherent).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int32_t x, int32_t y,
+                                                   int32_t z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // 3-D tiled TMA load of box (x, y, z) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t x,
                                             int32_t y, int32_t z, uint32_t bar, uint64_t policy)
