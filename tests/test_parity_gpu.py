@@ -306,3 +306,32 @@ def test_fused_decode_after_timeout_with_rezeroed_workspace(cuda_device):
     o_ref, lse_ref = _oracle(inp)
     assert_within(errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape),
                          lse_ref.reshape(lse.shape)), **TIGHT)
+
+
+def test_back_to_back_calls_match_isolated_calls(cuda_device):
+    """Splits longer than the stage ring prefetch their first keys into L2 and
+    let the next call launch before waiting for the previous one.  Calls on
+    alternating inputs, queued back to back on one stream and sharing one
+    workspace, give the bits of the same calls made one at a time."""
+    B, Hq, Hkv = 1, 32, 8
+    a = to_device(make_small(B, Hq, Hkv, 128, [16384], seed=91), cuda_device)
+    b = to_device(make_small(B, Hq, Hkv, 128, [16384], seed=92), cuda_device)
+    info = fd.plan(B, Hq, Hkv, 128, a["kv_indptr"])
+    split_keys = 16384 // info.total_splits
+    assert split_keys > 4 * 32, "the splits must be longer than the ring"
+    ws = torch.zeros(info.workspace_bytes, dtype=torch.uint8, device=cuda_device)
+
+    def call(x):
+        return fd.decode(x["q"], x["k"], x["v"], x["kv_indptr"], x["kv_indptr_dev"], x["scale"],
+                         workspace=ws)
+
+    ref = []
+    for x in (a, b):
+        ref.append(call(x))
+        torch.cuda.synchronize()
+    outs = [call(a if i % 2 == 0 else b) for i in range(24)]
+    torch.cuda.synchronize()
+    assert fd.get_device_status(ws) == 0
+    for i, (o, lse) in enumerate(outs):
+        o_ref, lse_ref = ref[i % 2]
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), f"call {i}"
