@@ -1062,6 +1062,21 @@ __device__ __forceinline__ void finish_item(const SplitParams &p, const Item &it
     group_sync<BAR>();
 }
 
+// L2 prefetch of one TMA box of K and one of V (KV head kvh) from row y:
+// the rows one stage copy of that box would read.
+template <class SG>
+__device__ __forceinline__ void prefetch_box(const CUtensorMap *tm_k, const CUtensorMap *tm_v, int kvh,
+                                             int32_t y)
+{
+    if constexpr (SG::kFp8) {
+        tma_prefetch_l2_2d(tm_k, kvh * kHeadDim, y);
+        tma_prefetch_l2_2d(tm_v, kvh * kHeadDim, y);
+    } else {
+        tma_prefetch_l2_3d(tm_k, 0, y, 2 * kvh);
+        tma_prefetch_l2_3d(tm_v, 0, y, 2 * kvh);
+    }
+}
+
 // One item per CTA: the grid is the items, all resident at once (the plan
 // fits one wave).  Warp NC produces, warps 0..NC-1 consume, and the whole CTA
 // closes the item.
@@ -1119,25 +1134,38 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         // prefetches would only delay them.  Measured (interleaved A/B): 64k
         // step 43.7 -> 40.0 us, 128k 79.7 -> 76.5 us, FP8 64k 27.4 -> 26.0 us;
         // 192 KB and 384 KB per CTA were each worse on some workload.
+        //  Paged: the lanes share the boxes of the prologue's keys, each looking
+        // up its box's page.  The page list is read through L2 only: the
+        // preceding grid may still be writing it, so a page id read here can
+        // be stale -- it then only misdirects a hint, and no stale line is
+        // left in L1 for the producer's own lookups after the wait.  Ids
+        // outside the pool are skipped.
         constexpr int kPrologueBytes = 256 * 1024;
         constexpr int kPrefetchTiles = kPrologueBytes / SG::kBytes;   // per CTA
-        if constexpr (!paged && !SG::kDirect) {
-            if (early_derive && found && lane == 0 && c.len > 0) {
+        if constexpr (!SG::kDirect) {
+            if (early_derive && found && c.len > 0) {   // warp-uniform
                 const int32_t len = split_len_for(c.len, c.splits);
                 const int32_t t0p = c.s * len;
-                const int n_split = (min(t0p + len, c.len) - t0p + kTile - 1) / kTile;
+                const int32_t t1p = min(t0p + len, c.len);
+                const int n_split = (t1p - t0p + kTile - 1) / kTile;
                 if (n_split > NS) {
-                    for (int i = 0; i < min(kPrefetchTiles, n_split); ++i) {
-                        const int32_t y = c.base + t0p + i * kTile;
-                        if constexpr (SG::kFp8) {
-                            tma_prefetch_l2_2d(&tm_k, kvh * kHeadDim, y);
-                            tma_prefetch_l2_2d(&tm_v, kvh * kHeadDim, y);
-                        } else {
-                            tma_prefetch_l2_3d(&tm_k, 0, y, 2 * kvh);
-                            tma_prefetch_l2_3d(&tm_v, 0, y, 2 * kvh);
+                    if constexpr (!paged) {
+                        if (lane == 0)
+                            for (int i = 0; i < min(kPrefetchTiles, n_split); ++i)
+                                prefetch_box<SG>(&tm_k, &tm_v, kvh, c.base + t0p + i * kTile);
+                    } else if (c.base >= 0 && c.base + c.pages <= p.num_page_entries) {
+                        constexpr int kBox = SG::kBoxRows;
+                        const int32_t t_end = min(t1p, t0p + kPrefetchTiles * kTile);
+                        for (int32_t t = t0p + lane * kBox; t < t_end; t += 32 * kBox) {
+                            const int32_t pg = t / p.page_size;
+                            const int32_t id = pg < c.pages ? __ldcg(p.page_indices + c.base + pg) : -1;
+                            if (id >= 0 && id < p.num_pages)
+                                prefetch_box<SG>(&tm_k, &tm_v, kvh, id * p.page_size + t % p.page_size);
                         }
                     }
-                    griddep_launch_dependents();
+                    __syncwarp();
+                    if (lane == 0)
+                        griddep_launch_dependents();
                 }
             }
         }
