@@ -60,3 +60,30 @@ def test_plan_paged_rejects_bad_layouts(page_size, last, code):
     with pytest.raises(fd.FdError) as e:
         fd.plan_paged(1, 8, 8, 128, page_size, [0, 2], last, num_sms=152)
     assert e.value.code == code
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 48, 64, 256])
+def test_paged_tiles_never_straddle_a_page(page_size):
+    # The paged kernels copy a tile as TMA boxes of 32 rows (P a multiple of
+    # 32) or 16 rows (otherwise), each addressed through one page-table entry,
+    # which is only right if no box crosses a page boundary: every split, and
+    # so every tile, must start at a key offset that is a multiple of the box.
+    rng = np.random.default_rng(page_size)
+    box = 32 if page_size % 32 == 0 else 16
+    for _ in range(20):
+        B = int(rng.integers(1, 12))
+        pages = rng.integers(0, 40, size=B)
+        last = np.where(pages > 0, rng.integers(1, page_size + 1, size=B), 0).astype(np.int32)
+        page_indptr = np.zeros(B + 1, dtype=np.int32)
+        page_indptr[1:] = np.cumsum(pages)
+        lens = np.where(pages > 0, (pages - 1) * page_size + last, 0)
+        ip = np.zeros(B + 1, dtype=np.int32)
+        ip[1:] = np.cumsum(lens)
+        for chunk in (0, 32, 96, 160):
+            info = fd.plan_paged(B, 32, 8, 128, page_size, page_indptr, last, num_sms=152,
+                                 chunk=chunk)
+            for b, _, _, t0, t1 in fd.plan_work_items(info, ip):
+                off = t0 - ip[b]
+                assert off % fd.TILE_TOKENS == 0
+                for k in range(off, t1 - ip[b], box):
+                    assert k % page_size + box <= page_size, "a box crosses into the next page"
