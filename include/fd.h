@@ -55,7 +55,11 @@
  * Launches: the kernels are launched with programmatic stream serialisation:
  * each may begin launching while the previous grid in the stream finishes,
  * and waits for that grid to complete before it reads or writes global
- * memory, so stream order is kept.
+ * memory, so stream order is kept.  The one exception changes no result:
+ * before that wait, the split kernel of a long split may prefetch the split's
+ * first K/V rows into L2 (a hint), and the paged one reads the page list
+ * through L2 to aim those prefetches.  Every value a kernel computes is read
+ * after the wait.
  */
 #ifndef FD_H
 #define FD_H
