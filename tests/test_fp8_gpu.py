@@ -13,8 +13,9 @@ import torch
 
 import oracle
 import split_kv_flashdecoding_gb300 as fd
+from tests import full_size
 from tests.parity_util import assert_within, errors
-from workloads import make_inputs, make_small, to_fp8, to_paged
+from workloads import WORKLOADS, make_small, to_fp8, to_paged
 
 pytestmark = pytest.mark.gpu
 
@@ -72,23 +73,15 @@ def test_fp8_q_of_any_magnitude(cuda_device, q_mult, k_mult):
     assert_within(err, what=f"q x {q_mult}")
 
 
-@pytest.mark.parametrize("idx", [1, 4], ids=["gqa_b1_h32x8_l65536", "stressed_b16_h64x8_l32768"])
+@pytest.mark.parametrize("idx", range(len(WORKLOADS)), ids=[w.name for w in WORKLOADS])
 def test_fp8_full_size(cuda_device, idx):
     """Full-size workloads quantised to FP8, in the launch configuration the
-    benchmark uses: sampled rows against the oracle."""
-    inp = make_inputs(idx)
-    f = to_fp8(inp)
-    w = inp["workload"]
+    benchmark uses: every row against the oracle, rel-L2 over the whole O."""
+    f = full_size.fp8_inputs(idx)
     o, lse = _run(f, cuda_device)
     torch.cuda.synchronize()
-    B, Hq, D = w.batch, w.num_qo_heads, w.head_dim
-    rows = np.random.default_rng(idx).permutation(B * Hq)[:32]
-    o_ref, lse_ref = oracle.decode_fp8(f["q"], f["k_fp8"], f["v_fp8"], f["k_scale"], f["v_scale"],
-                                       f["kv_indptr"], f["scale"], rows=rows)
-    o_h = o.reshape(B * Hq, D).cpu().numpy()[rows]
-    l_h = lse.reshape(B * Hq).cpu().numpy()[rows]
-    assert_within(errors(o_h, l_h, o_ref, lse_ref), what=w.name)
-    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    o_ref, lse_ref = full_size.reference_fp8(idx)
+    assert_within(errors(*full_size.as_rows(o, lse), o_ref, lse_ref), what=WORKLOADS[idx].name)
 
 
 @pytest.mark.parametrize("page_size", [16, 32, 48, 64])

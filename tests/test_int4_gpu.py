@@ -15,8 +15,9 @@ import torch
 
 import oracle
 import split_kv_flashdecoding_gb300 as fd
+from tests import full_size
 from tests.parity_util import assert_within, errors
-from workloads import make_inputs, make_small, random_int4, to_int4, to_paged_int4
+from workloads import WORKLOADS, make_small, random_int4, to_int4, to_paged_int4
 
 pytestmark = pytest.mark.gpu
 
@@ -66,22 +67,15 @@ def test_int4_decode_matches_oracle(cuda_device, name, B, Hq, Hkv, lengths, kind
     assert_within(err, **TIGHT, what=f"{name} {kind} (tight)")
 
 
-@pytest.mark.parametrize("idx", [1, 4], ids=["gqa_b1_h32x8_l65536", "stressed_b16_h64x8_l32768"])
+@pytest.mark.parametrize("idx", range(len(WORKLOADS)), ids=[w.name for w in WORKLOADS])
 def test_int4_full_size(cuda_device, idx):
     """Full-size workloads quantised to INT4, in the launch configuration the
-    benchmark uses: sampled rows against the oracle."""
-    inp = make_inputs(idx)
-    f = to_int4(inp)
-    w = inp["workload"]
+    benchmark uses: every row against the oracle, rel-L2 over the whole O."""
+    f = full_size.int4_inputs(idx)
     o, lse = _run(f, cuda_device)
     torch.cuda.synchronize()
-    B, Hq, D = w.batch, w.num_qo_heads, w.head_dim
-    rows = np.random.default_rng(idx).permutation(B * Hq)[:32]
-    o_ref, lse_ref = _ref(f, rows=rows)
-    o_h = o.reshape(B * Hq, D).cpu().numpy()[rows]
-    l_h = lse.reshape(B * Hq).cpu().numpy()[rows]
-    assert_within(errors(o_h, l_h, o_ref, lse_ref), what=w.name)
-    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    o_ref, lse_ref = full_size.reference_int4(idx)
+    assert_within(errors(*full_size.as_rows(o, lse), o_ref, lse_ref), what=WORKLOADS[idx].name)
 
 
 def _paged_call(pg, f, dev):

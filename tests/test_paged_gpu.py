@@ -12,8 +12,9 @@ import torch
 
 import oracle
 import split_kv_flashdecoding_gb300 as fd
+from tests import full_size
 from tests.parity_util import assert_within, errors, to_device
-from workloads import make_inputs, make_small, to_paged
+from workloads import make_small, to_paged
 
 pytestmark = pytest.mark.gpu
 
@@ -64,17 +65,15 @@ def test_paged_matches_oracle_and_ragged(cuda_device, page_size, name, B, Hq, Hk
 
 @pytest.mark.parametrize("page_size", [16, 64])
 def test_paged_full_size_64k(cuda_device, page_size):
-    """The 64k-context GQA workload (B=1, Hq=32, Hkv=8) in 16- and 64-key pages."""
-    inp = make_inputs(1)
+    """The 64k-context GQA workload (B=1, Hq=32, Hkv=8) in 16- and 64-key
+    pages: all 32 rows against the oracle."""
+    inp = full_size.inputs(1)
     pg = to_paged(inp, page_size, seed=11)
     d = _paged_dev(pg, cuda_device)
     o, lse = _decode_paged(pg, d)
     torch.cuda.synchronize()
-    rows = np.arange(0, 32, 3)
-    o_ref, lse_ref = oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"],
-                                   rows=rows)
-    assert_within(errors(o.reshape(32, 128).cpu().numpy()[rows], lse.reshape(32).cpu().numpy()[rows],
-                         o_ref, lse_ref), what=f"64k P={page_size}")
+    o_ref, lse_ref = full_size.reference(1)
+    assert_within(errors(*full_size.as_rows(o, lse), o_ref, lse_ref), what=f"64k P={page_size}")
 
 
 def test_page_index_outside_pool_is_flagged(cuda_device):
