@@ -139,3 +139,51 @@ def test_nan_in_unused_page_rows_does_not_leak(cuda_device, page_size):
     torch.cuda.synchronize()
     assert torch.isfinite(outs[1][0]).all() and torch.isfinite(outs[1][1]).all()
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_back_to_back_paged_calls_with_page_tables_rewritten_in_stream(cuda_device):
+    """Long paged splits read the page list through L2 and prefetch their first
+    pages before waiting for the preceding grid.  Here every call is preceded,
+    in the same stream and with no synchronisation, by kernels that rewrite the
+    page list and the page contents between two layouts (different keys and a
+    different page order): a page id read early may be stale, which may only
+    misdirect a prefetch.  The queued calls must give the bits of the same
+    calls made one at a time, with device status 0."""
+    B, Hq, Hkv, P = 1, 32, 8, 16
+    layouts = []
+    for seed in (93, 94):
+        inp = make_small(B, Hq, Hkv, 128, [16384], seed=seed)
+        layouts.append(to_paged(inp, P, seed=seed + 10))
+    info = fd.plan_paged(B, Hq, Hkv, 128, P, layouts[0]["kv_page_indptr"],
+                         layouts[0]["kv_last_page_len"])
+    split_keys = 16384 // info.total_splits
+    assert split_keys > 4 * 32, "the splits must be longer than the ring"
+    src = [_paged_dev(pg, cuda_device) for pg in layouts]
+    for name in ("kv_page_indptr", "kv_last_page_len"):
+        assert torch.equal(src[0][name], src[1][name])
+    live = {k: src[0][k].clone() for k in src[0]}
+    ws = torch.zeros(info.workspace_bytes, dtype=torch.uint8, device=cuda_device)
+
+    def load(x):   # elementwise kernels writing the live page list and pools
+        torch.add(src[x]["kv_page_indices"], 0, out=live["kv_page_indices"])
+        torch.mul(src[x]["k_pages"], 1, out=live["k_pages"])
+        torch.mul(src[x]["v_pages"], 1, out=live["v_pages"])
+        torch.mul(src[x]["q"], 1, out=live["q"])
+
+    ref = []
+    for x in (0, 1):
+        load(x)
+        torch.cuda.synchronize()
+        o, lse = _decode_paged(layouts[x], live, ws)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), lse.clone()))
+    assert not torch.equal(ref[0][0], ref[1][0])
+    outs = []
+    for i in range(24):
+        load(i % 2)
+        outs.append(_decode_paged(layouts[i % 2], live, ws))
+    torch.cuda.synchronize()
+    assert fd.get_device_status(ws) == 0
+    for i, (o, lse) in enumerate(outs):
+        o_ref, lse_ref = ref[i % 2]
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), f"call {i}"
