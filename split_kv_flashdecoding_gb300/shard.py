@@ -37,15 +37,23 @@ def local_indptr(starts, ends) -> np.ndarray:
 
 
 def gather_states(o, lse, group=None):
-    """All-gather every rank's (O, LSE) into [R, ...] tensors (rank order)."""
+    """All-gather every rank's (O, LSE) into [R, ...] tensors (rank order), on
+    o's device.  NCCL gathers device tensors in place; a gloo group (CPU
+    collectives) gets host copies and the result is copied back."""
     import torch
     import torch.distributed as dist
     world = dist.get_world_size(group)
-    os_ = [torch.empty_like(o) for _ in range(world)]
-    ls_ = [torch.empty_like(lse) for _ in range(world)]
-    dist.all_gather(os_, o.contiguous(), group=group)
-    dist.all_gather(ls_, lse.contiguous(), group=group)
-    return torch.stack(os_), torch.stack(ls_)
+    staged = o.is_cuda and dist.get_backend(group) == "gloo"
+    src_o = o.detach().cpu().contiguous() if staged else o.contiguous()
+    src_l = lse.detach().cpu().contiguous() if staged else lse.contiguous()
+    os_ = [torch.empty_like(src_o) for _ in range(world)]
+    ls_ = [torch.empty_like(src_l) for _ in range(world)]
+    dist.all_gather(os_, src_o, group=group)
+    dist.all_gather(ls_, src_l, group=group)
+    o_all, l_all = torch.stack(os_), torch.stack(ls_)
+    if staged:
+        o_all, l_all = o_all.to(o.device), l_all.to(lse.device)
+    return o_all, l_all
 
 
 def decode_sequence_sharded(q, k_shard, v_shard, local_indptr_host, local_indptr_dev, scale: float, *,

@@ -70,3 +70,61 @@ def test_logical_ranks_on_one_gpu(cuda_device, R, name, lengths):
     o_ref, lse_ref = oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"])
     err = errors(o.cpu().numpy(), lse.cpu().numpy(), o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
     assert_within(err, **TIGHT, what=f"{name} over {R} ranks")
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+SHARDED_LENGTHS = [9000, 1, 0, 3000, 64]   # request 1: rank 0's shard empty; request 2: no keys
+
+
+def _gpu_rank_main(rank, world, port, out_dir):
+    """One rank of the shipped sequence-sharded step: its own shard buffers on
+    cuda:0, fd_decode, the gloo all-gather of the states, fd_merge_states."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+        inp = make_small(len(SHARDED_LENGTHS), 32, 8, 128, SHARDED_LENGTHS, seed=77)
+        starts, ends = shard.shard_bounds(inp["kv_indptr"], world, rank)
+        rows = np.concatenate([np.arange(s, e) for s, e in zip(starts, ends)]).astype(np.int64)
+        loc = shard.local_indptr(starts, ends)
+        k = inp["k"][rows].to(dev)
+        v = inp["v"][rows].to(dev)
+        o, lse = shard.decode_sequence_sharded(inp["q"].to(dev), k, v, loc,
+                                               torch.from_numpy(loc).to(dev), inp["scale"])
+        torch.cuda.synchronize()
+        np.save(os.path.join(out_dir, f"o{rank}.npy"), o.cpu().numpy())
+        np.save(os.path.join(out_dir, f"lse{rank}.npy"), lse.cpu().numpy())
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sequence_sharded_step_two_processes(cuda_device, tmp_path):
+    """shard.decode_sequence_sharded as shipped: two processes on one GPU, each
+    holding half of every request's keys, exchange their states through a gloo
+    all-gather (host copies; no peer memory) and merge them with
+    fd_merge_states.  Both ranks get the same result, and every row matches the
+    oracle on the unsharded keys (an empty shard and an empty request
+    included)."""
+    import torch.multiprocessing as mp
+    world = 2
+    mp.spawn(_gpu_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    outs = [(np.load(tmp_path / f"o{r}.npy"), np.load(tmp_path / f"lse{r}.npy")) for r in range(world)]
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    inp = make_small(len(SHARDED_LENGTHS), 32, 8, 128, SHARDED_LENGTHS, seed=77)
+    o_ref, lse_ref = oracle.decode(inp["q"], inp["k"], inp["v"], inp["kv_indptr"], inp["scale"])
+    o, lse = outs[0]
+    err = errors(o, lse, o_ref.reshape(o.shape), lse_ref.reshape(lse.shape))
+    assert_within(err, **TIGHT, what="two processes")
+    assert np.all(o[2] == 0) and np.all(np.isneginf(lse[2]))
