@@ -31,7 +31,11 @@
  * FD_ERR_UNSUPPORTED.  q, k, v, o, partial_o must be 16-byte aligned.
  *
  * Ownership: the caller owns every buffer.  The library allocates no device
- * memory and keeps no state between calls besides a cached SM count per device.
+ * memory and keeps no state between calls besides a cached SM count per device,
+ * with one exception: fd_decode_static_workspace keeps its scratch in a fixed
+ * device array of FD_STATIC_WORKSPACE_BYTES inside the library (present on
+ * every GPU that loads it, holding the last such call's contents) and caches
+ * that array's device address per device.
  * All device work is asynchronous on the given stream (a cudaStream_t passed as
  * void*; NULL = legacy default stream).
  *
@@ -384,7 +388,10 @@ int fd_merge_states(int num_states, int rows, int head_dim, const float *o_state
  * arguments needs more than FD_STATIC_WORKSPACE_BYTES (fd_plan reports the
  * need in fd_plan_info.workspace_bytes); use fd_decode with a workspace then.
  * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture.  Each call
+ * device current and caches it for the life of the process; make that first
+ * call before any stream capture.  The cached address does not survive
+ * cudaDeviceReset (or any other teardown of the device's primary context):
+ * after one, this entry point must not be called again in the process.  Each call
  * clears the workspace header and the merge tickets on its stream before it runs.
  * All calls share the one array, which keeps the last call's contents: calls
  * that can overlap on the GPU (other streams, other host threads, without
