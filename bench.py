@@ -1,23 +1,29 @@
 """Benchmark of one split-KV decode-attention step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl fd|reference]
+                    [--impl fd|reference] [--kv-dtype bf16|fp8|int4] [--page-size P]
+                    [--graph] [--min-timed-ms MS] [--no-per-workload]
 
 A step is the whole path: one fd_decode call through the C ABI, i.e. the host
-plan (fd_plan), stage 1 (the split kernel) and stage 2 (the merge kernel), on
-one batch of seeded synthetic inputs already resident in HBM.  The default
+plan (fd_plan), stage 1 (the split kernel) and stage 2 (fused into it), on one
+batch of seeded synthetic inputs already resident in HBM.  The headline
 workload is the Llama-3-8B-shaped GQA decode at 64k context (B=1, Hq=32,
-Hkv=8, D=128, L=65536).  K steps run back to back between two CUDA events; the
-K/V a step reads is at least twice the L2 size (small workloads rotate through
-copies of their inputs), so no step is served from L2.  The split kernel is
-also timed alone (back to back), and each step once more one at a time after
-a 1 GiB L2 flush (that number includes launch latency and event overhead).
+Hkv=8, D=128, L=65536).  After W warm-up steps the K-step loop runs back to
+back inside one pair of CUDA events, repeated until the timed region lasts at
+least --min-timed-ms (200 ms); the K/V a step reads is at least twice the L2
+size (small workloads rotate through copies of their inputs), so no step is
+served from L2.  Stage 1 alone is also timed (back to back), and each step once
+more one at a time after a 1 GiB L2 flush (that number includes launch latency
+and event overhead).  Every other workload is then timed the same way, with
+the same kind of step, into `per_workload`.
 
 Prints one JSON line (rank 0).  `value` is achieved bandwidth in GB/s: the
 algorithmic bytes of a step (q + K + V + O + LSE + the partials written and
 read back) over the device time of the step; `ms_per_step` is that time.
-`--impl reference` times the fp64 CPU oracle on the host cores instead (a
-bounded sample of the same workload, extrapolated to one step).
+`roofline` is that of the step's one kernel (the split kernel with stage 2
+fused).  `--impl reference` times the fp64 CPU oracle on the host cores
+instead (a bounded sample of the same workload, extrapolated to one step),
+without loading the library.
 
 Multi-GPU (torchrun): every rank runs its own copy of the workload (requests
 are independent, no collective on the data path); value = all ranks' bytes /
@@ -106,6 +112,99 @@ def profiled_traffic(workload_name: str):
     return None if entry is None else entry.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------- partial rows of a plan
+
+TILE_TOKENS = 32        # keys per pipeline stage (FD_TILE_TOKENS)
+MIN_CHUNK = 128         # FD_MIN_CHUNK
+CTA_OVERHEAD_TILES = 3  # the planner's fixed per-CTA cost, in tiles
+CTAS_PER_SM = 2         # resident split-kernel CTAs per SM
+
+
+def _splits(L, c):
+    return -(-L // c) if L > 0 else 0
+
+
+def _split_len(L, n):
+    return -(-(-(-L // n)) // TILE_TOKENS) * TILE_TOKENS
+
+
+def plan_chunk(lengths, num_kv_heads: int, num_sms: int) -> int:
+    """The chunk length fd_plan picks (the rule include/fd.h documents): for
+    grids of 1, 2, 4 and 8 waves of resident CTAs, the chunk that sizes the
+    grid; keep the one whose dispatch, simulated in launch order onto the
+    resident-CTA slots, ends first (the fewest waves on a tie).  Host
+    bookkeeping only: the reference arm counts the partial bytes of the same
+    plan without loading the library."""
+    import heapq
+    slots = num_sms * CTAS_PER_SM
+    total = int(sum(lengths))
+
+    def chunk_for(target):
+        c = -(-(-(-total * num_kv_heads // target)) // TILE_TOKENS) * TILE_TOKENS
+        return min(max(c, MIN_CHUNK), 1 << 30)
+
+    def costs(c):
+        for L in lengths:
+            n = _splits(L, c)
+            if n:
+                sl = _split_len(L, n)
+                for s_ in range(n):
+                    keys = min(sl, L - s_ * sl)
+                    yield -(-keys // TILE_TOKENS) + CTA_OVERHEAD_TILES
+
+    best_c, best_t, last_c = chunk_for(slots), -1, -1
+    for waves in (1, 2, 4, 8):
+        c = chunk_for(slots * waves)
+        if c == last_c:
+            continue
+        last_c = c
+        cs = list(costs(c))
+        ctas = len(cs) * num_kv_heads
+        largest = max(cs, default=0)
+        if ctas <= slots:
+            t = largest
+        else:
+            lower = max(largest, -(-sum(cs) * num_kv_heads // slots))
+            if best_t >= 0 and lower >= best_t:
+                continue
+            free = [0] * slots       # each CTA takes the earliest free slot
+            heapq.heapify(free)
+            for cost in cs:          # the KV heads of one split, in a row
+                taken = []
+                for _ in range(num_kv_heads):
+                    if not free:         # more KV heads than slots: reuse the first ones
+                        for x in taken:
+                            heapq.heappush(free, x)
+                        taken = []
+                    taken.append(heapq.heappop(free) + cost)
+                for x in taken:
+                    heapq.heappush(free, x)
+            t = max(free)
+        if best_t < 0 or t < best_t:
+            best_t, best_c = t, c
+    return best_c
+
+
+def plan_partial_rows(lengths, num_qo_heads: int, num_kv_heads: int, num_sms: int) -> int:
+    c = plan_chunk(lengths, num_kv_heads, num_sms)
+    return sum(_splits(L, c) for L in lengths) * num_qo_heads
+
+
+def device_sm_count(default: int = 152) -> tuple[int, str]:
+    """SM count of GPU 0 from the CUDA driver (no context is created), or the
+    GB300's 152 when no driver answers."""
+    import ctypes
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        dev, n = ctypes.c_int(), ctypes.c_int()
+        if cu.cuInit(0) == 0 and cu.cuDeviceGet(ctypes.byref(dev), 0) == 0 and \
+                cu.cuDeviceGetAttribute(ctypes.byref(n), 16, dev) == 0 and n.value > 0:
+            return n.value, "CUDA driver"    # 16: CU_DEVICE_ATTRIBUTE_MULTIPROCESSOR_COUNT
+    except OSError:
+        pass
+    return default, "GB300 default"
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed loop runs."""
 
@@ -133,9 +232,14 @@ class ClockSampler:
 
     def mark(self):
         self.t_start = time.time()
+        self.t_end = None
+
+    def stop(self):
+        self.t_end = time.time()
 
     def __exit__(self, *exc):
-        self.t_end = time.time()
+        if getattr(self, "t_end", None) is None:
+            self.t_end = time.time()
         if self.proc:
             time.sleep(0.1)
             self.proc.terminate()
@@ -209,20 +313,16 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ fd arm
 
-def run_fd(args, world, rank, local) -> dict | None:
+def build_case(w, args, dev, rank, fd):
+    """One workload's inputs on the device and the step bench.py times: an
+    fd_decode call (or its paged / FP8 / INT4 / graph form) through the C ABI.
+    Returns a dict with the step, its bytes and everything the timings need."""
     import ctypes
 
     import torch
 
-    import split_kv_flashdecoding_gb300 as fd
     from workloads import make_inputs, to_fp8, to_int4, to_paged, to_paged_int4
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    w = workload(args.workload)
     inp = make_inputs(w.index, seed=rank_seed(w.index, rank))
     B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
     ip_host = np.ascontiguousarray(inp["kv_indptr"].numpy().astype(np.int32))
@@ -256,6 +356,7 @@ def run_fd(args, world, rank, local) -> dict | None:
         inp = dict(inp, k=f["k_int4"], v=f["v_int4"], k_scale=f["k_scale_int4"],
                    v_scale=f["v_scale_int4"], int4=True)
         del f
+    pg_ip = pg_last = None
     if paged:   # the same keys in a paged KV cache (scattered pages)
         pg = to_paged(inp, args.page_size, seed=13)
         bufs = [tuple(pg[x].to(dev) for x in ("q", "k_pages", "v_pages")) for _ in range(copies)]
@@ -268,19 +369,14 @@ def run_fd(args, world, rank, local) -> dict | None:
         del pg
     else:
         bufs = [tuple(inp[x].to(dev) for x in ("q", "k", "v")) for _ in range(copies)]
-    q, k, v = bufs[0]
 
     info0 = (fd.plan_paged(B, Hq, Hkv, D, args.page_size, pg_ip, pg_last) if paged
              else fd.plan(B, Hq, Hkv, D, ip_host))
     rows = info0.num_partial_rows
     nb = step_bytes(B, Hq, Hkv, D, T, rows, row_bytes)
-    ws_split = torch.zeros(fd.WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=dev)
-    po = torch.empty((rows, D), dtype=torch.float32, device=dev)
-    pl = torch.empty((rows,), dtype=torch.float32, device=dev)
     o = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     ws = torch.zeros(info0.workspace_bytes, dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     lib = fd.lib()
     P = ctypes.c_void_p
@@ -311,17 +407,31 @@ def run_fd(args, world, rank, local) -> dict | None:
                       P(vc.data_ptr()), ctypes.c_float(scale), P(o.data_ptr()), P(lse.data_ptr()),
                       P(ws.data_ptr()), ws.numel(), sp) for qc, kc, vc in bufs]
         step_fn, step_name = lib.fd_decode, "fd_decode"
-    split_args = [(ctypes.byref(info0), P(qc.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()),
-                   P(ip_dev.data_ptr()), ctypes.c_float(scale), P(po.data_ptr()),
-                   P(pl.data_ptr()), P(ws_split.data_ptr()), ws_split.numel(), sp)
-                  for qc, kc, vc in bufs]
 
     def step(i):
         rc = step_fn(*step_args[i % copies])
         if rc != 0:
             raise fd.FdError(rc, step_name)
 
+    # stage 1 alone (fd_decode_split) on the same inputs: a diagnostic of the
+    # ragged bf16 path (the other paths have no separate stage-1 entry point)
+    split = None
+    if not (paged or quant or args.graph):
+        ws_split = torch.zeros(fd.WORKSPACE_HEADER_BYTES, dtype=torch.uint8, device=dev)
+        po = torch.empty((rows, D), dtype=torch.float32, device=dev)
+        pl = torch.empty((rows,), dtype=torch.float32, device=dev)
+        split_args = [(ctypes.byref(info0), P(qc.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()),
+                       P(ip_dev.data_ptr()), ctypes.c_float(scale), P(po.data_ptr()),
+                       P(pl.data_ptr()), P(ws_split.data_ptr()), ws_split.numel(), sp)
+                      for qc, kc, vc in bufs]
+
+        def split(i):
+            rc = lib.fd_decode_split(*split_args[i % copies])
+            if rc != 0:
+                raise fd.FdError(rc, "fd_decode_split")
+
     info_g = None
+    step_calls = 1   # steps per step() call
     if args.graph:
         # GRAPH_STEPS fd_decode_graph steps per input copy captured in one CUDA
         # graph (device-side plan for a capacity of exactly this batch's keys),
@@ -347,166 +457,281 @@ def run_fd(args, world, rank, local) -> dict | None:
             graphs.append(g)
         ws = ws_g
         step_name = "fd_decode_graph"
+        step_calls = GRAPH_STEPS
 
         def step(i):   # GRAPH_STEPS steps
             graphs[i % copies].replay()
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize(dev)
-    if fd.get_device_status(ws) != 0:
-        raise RuntimeError("device status set during warm-up")
-
-    step_calls = GRAPH_STEPS if args.graph else 1   # steps per step() call
-    K = max(1, args.steps // step_calls) * step_calls
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        clocks.mark()
-        torch.cuda._sleep(2_000_000)        # lets the host queue steps ahead of the GPU
-        t_wall0 = time.perf_counter()
-        ev0.record(stream)
-        for i in range(K // step_calls):
-            step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall0
-        barrier(world)
+    # one item per CTA when the plan fits a wave of resident CTAs, else persistent
+    work = info_g.num_work if args.graph else info0.num_work   # the graph plan's capacity
+    persistent = work > info0.num_sms * info0.ctas_per_sm
+    kernel = ("split_kv_persistent_kernel" if persistent else "split_kv_kernel") + \
+        ("<fp8>" if fp8 else "<int4>" if int4 else "<bf16>")
     # stage 2 runs inside the split kernel; the merge kernel is launched only
     # when some request has no keys
     any_empty = bool(np.any(np.diff(ip_host) == 0))
-    launches = K * (int(info0.num_work > 0) + int(any_empty))
-    status = fd.get_device_status(ws)
+    launches_per_step = int(info0.num_work > 0) + int(any_empty)
+    return dict(w=w, inp=inp, ip_host=ip_host, ip_dev=ip_dev, bufs=bufs, copies=copies,
+                info=info0, nb=nb, o=o, lse=lse, ws=ws, stream=stream, step=step, split=split,
+                step_name=step_name, step_calls=step_calls, kernel=kernel,
+                launches_per_step=launches_per_step, paged=paged, fp8=fp8, int4=int4, T=T)
+
+
+def measure_case(case, args, world, dev, flush, clocks=None, n_flushed=100) -> dict:
+    """Time one workload's step: W warm-up steps; then the K-step loop, repeated
+    back to back (one pair of CUDA events around all of it) until the timed
+    region lasts at least --min-timed-ms; stage 1 alone; single steps after an
+    L2 flush."""
+    import torch
+
+    import split_kv_flashdecoding_gb300 as fd
+
+    stream, step, calls = case["stream"], case["step"], case["step_calls"]
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if fd.get_device_status(case["ws"]) != 0:
+        raise RuntimeError("device status set during warm-up")
+    K = max(1, args.steps // calls) * calls
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    # how many back-to-back repeats of the K-step loop fill the timed region
+    n_est = max(1, min(K, 50) // calls)
+    torch.cuda._sleep(1_000_000)
+    ev0.record(stream)
+    for i in range(n_est):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    est_ms = ev0.elapsed_time(ev1) / (n_est * calls)
+    rounds = max(1, math.ceil(args.min_timed_ms / max(K * est_ms, 1e-6)))
+    rounds = int(max_over_ranks(float(rounds), world, dev))
+
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if clocks is not None:
+        clocks.mark()
+    torch.cuda._sleep(2_000_000)        # lets the host queue steps ahead of the GPU
+    t_wall0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(rounds * K // calls):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    if clocks is not None:
+        clocks.stop()
+    barrier(world)
+    status = fd.get_device_status(case["ws"])
     if status != 0:
         raise RuntimeError(f"device status {fd.status_string(status)}")
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / K, world, dev)
+    timed_ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(timed_ms / (rounds * K), world, dev)
 
-    # The dominant kernel alone (stage 1), back to back on the same stream.
-    # A paged, FP8 or INT4 step has no separate stage-1 entry point: its one
-    # kernel is the step.
-    one_kernel = paged or quant or args.graph
-    if one_kernel:
-        split_avg = ms
-    else:
-        n_split = min(K, 500)
+    # stage 1 alone, back to back on the same stream (ragged bf16 only)
+    split_ms = None
+    if case["split"] is not None:
+        n_split = 500
         torch.cuda._sleep(2_000_000)
         ev0.record(stream)
         for i in range(n_split):
-            rc = lib.fd_decode_split(*split_args[i % copies])
-            if rc != 0:
-                raise fd.FdError(rc, "fd_decode_split")
+            case["split"](i)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
-        split_avg = ev0.elapsed_time(ev1) / n_split
+        split_ms = ev0.elapsed_time(ev1) / n_split
 
     # The same step timed one at a time after an L2 flush (includes each
     # step's launch latency and about 2 us of event overhead).
-    n_fl = min(K, 100)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_fl)]
-    for i in range(n_fl):
+           for _ in range(n_flushed)]
+    for i in range(n_flushed):
         flush.fill_(float(i))
         evs[i][0].record(stream)
         step(0)
         evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    flushed_ms = np.array([a.elapsed_time(b) for a, b in evs]) / step_calls
+    flushed_ms = np.array([a.elapsed_time(b) for a, b in evs]) / calls
+    return dict(K=K, rounds=rounds, ms=ms, timed_ms=timed_ms, wall_s=t_wall, split_ms=split_ms,
+                flushed_ms=flushed_ms, launches=rounds * K * case["launches_per_step"])
 
-    # end to end through the public API with host buffers: pinned H2D of the
-    # step's inputs, fd_decode, D2H of O and LSE, all inside the events
+
+def workload_summary(case, m, world, peak) -> dict:
+    """The per-workload entry of the JSON line."""
+    nb, info = case["nb"], case["info"]
+    gbs = aggregate_gbs(nb["step"], world, m["ms"])
+    return {
+        "us_per_step": round(m["ms"] * 1e3, 2),
+        "gbs": round(gbs, 1),
+        "frac_of_measured": round(gbs / world / peak, 4),
+        "frac_of_nominal_8tbs": round(gbs / world / NOMINAL_HBM_GBS, 4),
+        "split_only_us": None if m["split_ms"] is None else round(m["split_ms"] * 1e3, 2),
+        "step_us_after_l2_flush_p50": round(float(np.percentile(m["flushed_ms"], 50)) * 1e3, 2),
+        "timed_steps": m["rounds"] * m["K"],
+        "timed_region_ms": round(m["timed_ms"], 1),
+        "algorithmic_bytes_per_step": nb["step"],
+        "total_tokens": case["T"], "chunk": info.chunk, "splits": info.total_splits,
+        "ctas": info.num_work, "kernel": case["kernel"],
+    }
+
+
+def e2e_measure(case, args, world, dev, flush) -> dict:
+    """End to end through the public API with host buffers: pinned H2D of the
+    step's inputs, fd_decode, D2H of O and LSE, all inside the events."""
+    import torch
+
+    import split_kv_flashdecoding_gb300 as fd
+
+    inp, w, info, stream = case["inp"], case["w"], case["info"], case["stream"]
+    B, Hq, D = w.batch, w.num_qo_heads, w.head_dim
+    q_h, k_h, v_h = (inp[x].pin_memory() for x in ("q", "k", "v"))
+    ip_h = inp["kv_indptr"].pin_memory()
+    o_h = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    l_h = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    wsd = torch.zeros(info.workspace_bytes, dtype=torch.uint8, device=dev)
+    e2e_steps = max(3, min(args.steps, 20))
+    q, k, v = case["bufs"][0]
+    o, lse, ip_dev = case["o"], case["lse"], case["ip_dev"]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.fill_(float(i))
+        if i >= 2:
+            evs[i - 2][0].record(stream)
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        ip_dev.copy_(ip_h, non_blocking=True)
+        fd.decode(q, k, v, case["ip_host"], ip_dev, inp["scale"], o=o, lse=lse, workspace=wsd,
+                  stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+        if i >= 2:
+            evs[i - 2][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evs])), world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, ip_h))
+    d2h = sum(t.numel() * t.element_size() for t in (o_h, l_h))
+    return {"value": round(world * case["nb"]["step"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_fd(args, world, rank, local) -> dict | None:
+    import torch
+
+    import split_kv_flashdecoding_gb300 as fd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peak, peak_kind = measured_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    w = workload(args.workload)
+
+    # the headline workload: timed step with clocks, e2e, the CPU baseline
+    case = build_case(w, args, dev, rank, fd)
+    with ClockSampler(local) as clocks:
+        m = measure_case(case, args, world, dev, flush, clocks=clocks)
+    summary = workload_summary(case, m, world, peak)
     e2e = None
-    if not args.no_e2e and not one_kernel:
-        q_h, k_h, v_h = (inp[x].pin_memory() for x in ("q", "k", "v"))
-        ip_h = inp["kv_indptr"].pin_memory()
-        o_h = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
-        l_h = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
-        wsd = torch.zeros(info0.workspace_bytes, dtype=torch.uint8, device=dev)
-        e2e_steps = max(3, min(K, 20))
-        q, k, v = bufs[0]
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(e2e_steps)]
-        for i in range(e2e_steps + 2):
-            flush.fill_(float(i))
-            if i >= 2:
-                evs[i - 2][0].record(stream)
-            q.copy_(q_h, non_blocking=True)
-            k.copy_(k_h, non_blocking=True)
-            v.copy_(v_h, non_blocking=True)
-            ip_dev.copy_(ip_h, non_blocking=True)
-            fd.decode(q, k, v, ip_host, ip_dev, scale, o=o, lse=lse, workspace=wsd, stream=stream)
-            o_h.copy_(o, non_blocking=True)
-            l_h.copy_(lse, non_blocking=True)
-            if i >= 2:
-                evs[i - 2][1].record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evs])), world, dev)
-        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, ip_h))
-        d2h = sum(t.numel() * t.element_size() for t in (o_h, l_h))
-        e2e = {"value": round(world * nb["step"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+    if not args.no_e2e and not (case["paged"] or case["fp8"] or case["int4"] or args.graph):
+        e2e = e2e_measure(case, args, world, dev, flush)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1 and rank == 0:
+        cpu = cpu_baseline(w, case["inp"], case["nb"]["step"], budget_s=args.cpu_budget)
+    info, nb, ms = case["info"], case["nb"], m["ms"]
+    launches = m["launches"]
+    del case
+    torch.cuda.empty_cache()
+
+    # every other workload, the same step kind, each timed the same way
+    per_workload = {w.name: summary}
+    if not args.no_per_workload:
+        for other in WORKLOADS:
+            if other.name == w.name:
+                continue
+            c = build_case(other, args, dev, rank, fd)
+            mo = measure_case(c, args, world, dev, flush, n_flushed=50)
+            per_workload[other.name] = workload_summary(c, mo, world, peak)
+            del c
+            torch.cuda.empty_cache()
+    per_workload = {x.name: per_workload[x.name] for x in WORKLOADS if x.name in per_workload}
 
     if rank != 0:
         return None
-    peak, peak_kind = measured_peaks()
-    kernel_bytes = nb["step"] if one_kernel else nb["split"]
-    # one item per CTA when the plan fits a wave of resident CTAs, else persistent
-    work = info_g.num_work if args.graph else info0.num_work   # the graph plan's capacity
-    persistent = work > info0.num_sms * info0.ctas_per_sm
-    kernel_name = ("split_kv_persistent_kernel" if persistent else "split_kv_kernel") + \
-        ("<fp8>" if fp8 else "<int4>" if int4 else "<bf16>")
-    achieved = kernel_bytes / (split_avg * 1e-3) / 1e9
-    traffic = None if one_kernel else profiled_traffic(w.name)
     gbs = aggregate_gbs(nb["step"], world, ms)
+    # The dominant kernel is the one the step launches (the split kernel, with
+    # stage 2 fused): its launches are the timed steps, back to back.
+    achieved = nb["step"] / (ms * 1e-3) / 1e9
+    traffic = None
+    if not (args.kv_dtype != "bf16" or args.page_size or args.graph):
+        traffic = profiled_traffic(w.name)
     line = {
         "metric": METRIC,
         "value": round(gbs, 2),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": K,
+        "steps": m["K"],
         "warmup": args.warmup,
         "ms_per_step": round(ms, 5),
         "us_per_step": round(ms * 1e3, 2),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("bf16 q, fp8 e4m3 K/V widened to f16, fp32 accumulate/out" if fp8
-                  else "bf16 q, int4 K/V widened to bf16, fp32 scales/accumulate/out" if int4
-                  else "bf16 in, fp32 accumulate/out"),
+        "dtype": ("bf16 q, fp8 e4m3 K/V widened to f16, fp32 accumulate/out" if args.kv_dtype == "fp8"
+                  else "bf16 q, int4 K/V widened to bf16, fp32 scales/accumulate/out"
+                  if args.kv_dtype == "int4" else "bf16 in, fp32 accumulate/out"),
         "data": "synthetic (seeded, see workloads/)",
-        "config": {"workload": w.name, "description": w.description, "batch": B,
-                   "num_qo_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "total_tokens": T,
-                   "chunk": info0.chunk, "splits": info0.total_splits, "ctas": info0.num_work,
-                   "ctas_per_sm": info0.ctas_per_sm, "num_sms": info0.num_sms,
+        "config": {"workload": w.name, "description": w.description, "batch": w.batch,
+                   "num_qo_heads": w.num_qo_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "total_tokens": summary["total_tokens"],
+                   "chunk": info.chunk, "splits": info.total_splits, "ctas": info.num_work,
+                   "ctas_per_sm": info.ctas_per_sm, "num_sms": info.num_sms,
                    "l2": ("steps back to back; inputs larger than L2 (K/V of each step "
-                          f">= 2x L2, {copies} input cop{'y' if copies == 1 else 'ies'} rotated)"),
+                          ">= 2x L2, input copies rotated when a workload is smaller)"),
+                   "timed_rounds": m["rounds"],
+                   "timed_steps": m["rounds"] * m["K"],
+                   "timed_region_ms": round(m["timed_ms"], 1),
+                   "timing": (f"the {m['K']}-step loop repeated {m['rounds']}x back to back "
+                              "inside one pair of CUDA events, so the timed region lasts at "
+                              f"least {args.min_timed_ms:g} ms"),
                    "algorithmic_bytes_per_step": nb["step"],
                    "frac_of_nominal_8tbs": round(gbs / world / NOMINAL_HBM_GBS, 4),
-                   "split_us": round(split_avg * 1e3, 2),
+                   "split_only_us": summary["split_only_us"],
                    "step_us_after_l2_flush_p10_p50_p90": [
-                       round(float(np.percentile(flushed_ms, p)) * 1e3, 2) for p in (10, 50, 90)],
-                   "wall_s": round(t_wall, 3),
+                       round(float(np.percentile(m["flushed_ms"], p)) * 1e3, 2) for p in (10, 50, 90)],
+                   "wall_s": round(m["wall_s"], 3),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "kv_layout": (f"paged, page_size {args.page_size}, pages scattered in a pool"
-                                 if paged else "ragged packed"),
+                                 if args.page_size else "ragged packed"),
                    "kv_dtype": ("fp8 e4m3, one fp32 scale per KV head for K and for V"
-                                if fp8 else
+                                if args.kv_dtype == "fp8" else
                                 "int4 (two's complement, 2 per byte), one fp32 scale per key row "
-                                "and KV head for K and for V" if int4 else "bf16"),
+                                "and KV head for K and for V" if args.kv_dtype == "int4" else "bf16"),
                    "launch": ("CUDA graph replay of fd_decode_graph (device-side plan)"
                               if args.graph else "C ABI call per step (host plan)")},
-        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": summary["kernel"], "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "algorithmic_bytes_per_launch": kernel_bytes,
-                     "traffic": traffic},
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "algorithmic_bytes_per_launch": nb["step"],
+                     "launch_us": round(ms * 1e3, 2),
+                     "how": ("the step's one kernel (stage 1 with stage 2 fused): algorithmic "
+                             "bytes per launch / its average launch time over the timed steps"),
+                     "traffic": traffic,
+                     "split_only": None if m["split_ms"] is None else {
+                         "kernel": "fd_decode_split (stage 1 alone, diagnostic)",
+                         "us": round(m["split_ms"] * 1e3, 2),
+                         "achieved": round(nb["split"] / (m["split_ms"] * 1e-3) / 1e9, 1),
+                         "frac": round(nb["split"] / (m["split_ms"] * 1e-3) / 1e9 / peak, 4)}},
+        "per_workload": per_workload,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
         "e2e": e2e,
     }
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, inp, nb["step"], budget_s=args.cpu_budget)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     return line
 
 
@@ -561,13 +786,14 @@ def run_reference(args, world, rank) -> dict | None:
     minute and a half) and is extrapolated to the full step."""
     if rank != 0:
         return None
-    import split_kv_flashdecoding_gb300 as fd   # host planner only: counts the partial bytes
     from workloads import make_inputs
     w = workload(args.workload)
     inp = make_inputs(w.index)
     B, Hq, Hkv, D = w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim
     T = int(inp["kv_indptr"][-1])
-    rows_partial = fd.plan(B, Hq, Hkv, D, inp["kv_indptr"], num_sms=152).num_partial_rows
+    # the fd arm's step bytes: the same plan's partials, counted on the host
+    num_sms, sm_source = device_sm_count()
+    rows_partial = plan_partial_rows(inp["lengths"], Hq, Hkv, num_sms)
     nb = step_bytes(B, Hq, Hkv, D, T, rows_partial)
     cores = max(1, len(os.sched_getaffinity(0)))
     all_rows = B * Hq
@@ -586,7 +812,10 @@ def run_reference(args, world, rank) -> dict | None:
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, see workloads/)",
-        "config": {"workload": w.name, "description": w.description},
+        "config": {"workload": w.name, "description": w.description,
+                   "algorithmic_bytes_per_step": nb["step"],
+                   "bytes_counted_as": (f"the fd arm's step bytes (q + K + V + O + LSE + partials "
+                                        f"of its plan for {num_sms} SMs, {sm_source})")},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{n} of {all_rows} (request, query-head) rows of {w.name} "
@@ -611,6 +840,11 @@ def main():
                          "four-bit codes with per-row scales (fd_decode_int4)")
     ap.add_argument("--page-size", type=int, default=0,
                     help="time fd_decode_paged on the same keys laid out as a paged KV cache")
+    ap.add_argument("--min-timed-ms", type=float, default=200.0,
+                    help="the K-step loop is repeated back to back until the timed region "
+                         "lasts at least this long")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only --workload (default: every workload, the same step kind)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

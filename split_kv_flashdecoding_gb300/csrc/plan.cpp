@@ -92,6 +92,11 @@ int64_t simulate_makespan(int batch, const int32_t *indptr, int num_kv_heads, in
             int64_t need = num_kv_heads;   // the KV heads of one split, in a row
             taken.clear();
             while (need > 0) {
+                if (free_at.empty()) {   // more KV heads than slots: reuse the first ones
+                    for (const auto &t : taken)
+                        free_at[t.first] += t.second;
+                    taken.clear();
+                }
                 auto it = free_at.begin();
                 const int64_t k = std::min(need, it->second);
                 taken.emplace_back(it->first + cost, k);

@@ -193,3 +193,30 @@ def test_plan_rejects_bad_chunk():
     with pytest.raises(fd.FdError) as e:
         fd.plan(1, 8, 8, 128, [0, 100], num_sms=152, chunk=48)
     assert e.value.code == -1
+
+
+@pytest.mark.parametrize("num_sms", [152, 132, 7, 3, 1])
+def test_bench_host_plan_rule_matches_fd_plan(num_sms):
+    """bench.py's reference arm counts the partial bytes of fd_plan's plan
+    without loading the library, from the rule include/fd.h documents: the
+    same chunk on the five workloads and on random ragged batches, including
+    plans with more KV heads than resident-CTA slots."""
+    import bench
+    from workloads import WORKLOADS
+    rng = np.random.default_rng(num_sms)
+    cases = []
+    for w in WORKLOADS:
+        lengths = (np.random.default_rng(42 + w.index).integers(w.ragged[0], w.ragged[1] + 1, w.batch)
+                   if w.ragged else [w.kv_len] * w.batch)
+        cases.append(([int(x) for x in lengths], w.num_qo_heads, w.num_kv_heads))
+    for _ in range(60):
+        B = int(rng.integers(1, 70))
+        lengths = rng.integers(0, 40000, B) * (rng.random(B) > 0.1)
+        hkv = int(rng.choice([1, 2, 8]))
+        cases.append(([int(x) for x in lengths], hkv * int(rng.choice([1, 2, 4, 8])), hkv))
+    for lengths, hq, hkv in cases:
+        ip = np.zeros(len(lengths) + 1, dtype=np.int32)
+        ip[1:] = np.cumsum(lengths)
+        info = fd.plan(len(lengths), hq, hkv, 128, ip, num_sms=num_sms)
+        assert bench.plan_chunk(lengths, hkv, num_sms) == info.chunk
+        assert bench.plan_partial_rows(lengths, hq, hkv, num_sms) == info.num_partial_rows
