@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <algorithm>
 #include <vector>
@@ -118,6 +119,41 @@ cudaStream_t as_stream(void *s)
     return reinterpret_cast<cudaStream_t>(s);
 }
 
+// A token unique to each fused call (never 0, the value of a zeroed flag):
+// the split kernel's CTAs publish their partial rows by writing it into their
+// flags, so flags left by earlier calls never match.
+int32_t next_call_token()
+{
+    static std::atomic<uint32_t> counter{0};
+    uint32_t t = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (t == 0)
+        t = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    return static_cast<int32_t>(t);
+}
+
+// Where fd_decode keeps its scratch in a workspace of a plan:
+// status header | tickets [B * Hkv] | partial LSE | partial O | flags [num_work].
+struct WorkspaceLayout {
+    int *counters;
+    float *partial_lse;
+    float *partial_o;
+    int *flags;
+};
+
+WorkspaceLayout workspace_layout(void *workspace, int64_t batch, int64_t num_kv_heads,
+                                 int64_t num_partial_rows)
+{
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    WorkspaceLayout l;
+    l.counters = reinterpret_cast<int *>(ws + FD_WORKSPACE_HEADER_BYTES);
+    uint8_t *after = ws + FD_WORKSPACE_HEADER_BYTES + round_up(batch * num_kv_heads * 4, 256);
+    l.partial_lse = reinterpret_cast<float *>(after);
+    uint8_t *po = after + round_up(num_partial_rows * 4, 256);
+    l.partial_o = reinterpret_cast<float *>(po);
+    l.flags = reinterpret_cast<int *>(po + num_partial_rows * kHeadDim * 4);
+    return l;
+}
+
 }  // namespace
 
 extern "C" const char *fd_status_string(int status)
@@ -189,7 +225,7 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
                   void *workspace, float *o, float *lse, int *counters,
                   const int32_t *kv_indptr_host, cudaStream_t stream,
                   const PagedKV *paged = nullptr, const QuantKV *quant = nullptr,
-                  bool device_plan = false)
+                  bool device_plan = false, int *flags = nullptr)
 {
     if (!q || !k || !v || !kv_indptr_dev || !partial_o || !partial_lse)
         return FD_ERR_INVALID_ARG;
@@ -239,6 +275,8 @@ int launch_stage1(const fd_plan_info *info, const void *q, const void *k, const 
     p.o = o;
     p.lse = lse;
     p.counters = counters;
+    p.flags = counters && !device_plan ? flags : nullptr;
+    p.token = p.flags ? next_call_token() : 0;
     // kv_indptr_host is only known on the fd_decode path (the same values as
     // the device copy, by contract).
     p.indptr_in_params = kv_indptr_host && info->batch + 1 <= fd::kParamIndptr &&
@@ -339,17 +377,14 @@ int decode_ragged(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
         return FD_OK;
     if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4) || !kv_indptr_dev)
         return FD_ERR_INVALID_ARG;
-    // workspace: status header | tickets [B * Hkv] | partial LSE | partial O
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    int *counters = reinterpret_cast<int *>(ws + FD_WORKSPACE_HEADER_BYTES);
-    uint8_t *after = ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)batch * num_kv_heads * 4, 256);
-    float *partial_lse = reinterpret_cast<float *>(after);
-    float *partial_o =
-        reinterpret_cast<float *>(after + round_up((int64_t)info.num_partial_rows * 4, 256));
+    const WorkspaceLayout wl = workspace_layout(workspace, batch, num_kv_heads, info.num_partial_rows);
+    int *counters = wl.counters;
+    float *partial_lse = wl.partial_lse;
+    float *partial_o = wl.partial_o;
     cudaStream_t s = as_stream(stream);
     if (info.num_work > 0) {
         rc = launch_stage1(&info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace,
-                           o, lse, counters, kv_indptr_host, s, nullptr, quant);
+                           o, lse, counters, kv_indptr_host, s, nullptr, quant, false, wl.flags);
         if (rc != FD_OK)
             return rc;
     }
@@ -446,19 +481,17 @@ int decode_paged(int batch, int num_qo_heads, int num_kv_heads, int head_dim, in
         return FD_ERR_INVALID_ARG;
     if (num_pages <= 0 || (int64_t)num_pages * page_size > INT32_MAX)
         return FD_ERR_INVALID_ARG;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    int *counters = reinterpret_cast<int *>(ws + FD_WORKSPACE_HEADER_BYTES);
-    uint8_t *after = ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)batch * num_kv_heads * 4, 256);
-    float *partial_lse = reinterpret_cast<float *>(after);
-    float *partial_o =
-        reinterpret_cast<float *>(after + round_up((int64_t)info.num_partial_rows * 4, 256));
+    const WorkspaceLayout wl = workspace_layout(workspace, batch, num_kv_heads, info.num_partial_rows);
+    int *counters = wl.counters;
+    float *partial_lse = wl.partial_lse;
+    float *partial_o = wl.partial_o;
     cudaStream_t s = as_stream(stream);
     if (info.num_work > 0) {
         const PagedKV pk{page_size, num_pages, kv_last_page_len_dev, kv_last_page_len_host,
                          kv_page_indices_dev, kv_page_indptr_host[batch]};
         rc = launch_stage1(&info, q, k_pages, v_pages, kv_page_indptr_dev, scale, partial_o,
                            partial_lse, workspace, o, lse, counters, kv_page_indptr_host, s, &pk,
-                           quant);
+                           quant, false, wl.flags);
         if (rc != FD_OK)
             return rc;
     }
@@ -615,15 +648,10 @@ extern "C" int fd_decode_graph(const fd_plan_info *info, const int32_t *kv_indpt
         return FD_OK;
     if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4) || !kv_indptr_dev)
         return FD_ERR_INVALID_ARG;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    int *counters = reinterpret_cast<int *>(ws + FD_WORKSPACE_HEADER_BYTES);
-    uint8_t *after =
-        ws + FD_WORKSPACE_HEADER_BYTES + round_up((int64_t)info->batch * info->num_kv_heads * 4, 256);
-    float *partial_lse = reinterpret_cast<float *>(after);
-    float *partial_o =
-        reinterpret_cast<float *>(after + round_up((int64_t)info->num_partial_rows * 4, 256));
-    return launch_stage1(info, q, k, v, kv_indptr_dev, scale, partial_o, partial_lse, workspace, o,
-                         lse, counters, nullptr, as_stream(stream), nullptr, nullptr, true);
+    const WorkspaceLayout wl =
+        workspace_layout(workspace, info->batch, info->num_kv_heads, info->num_partial_rows);
+    return launch_stage1(info, q, k, v, kv_indptr_dev, scale, wl.partial_o, wl.partial_lse, workspace,
+                         o, lse, wl.counters, nullptr, as_stream(stream), nullptr, nullptr, true);
 }
 
 extern "C" int fd_merge_states(int num_states, int rows, int head_dim, const float *o_states,

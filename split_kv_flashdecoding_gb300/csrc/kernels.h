@@ -33,6 +33,13 @@ struct SplitParams {
     float *o;                   // [B, Hq, D]
     float *lse;                 // [B, Hq]
     int *counters;
+    // One-item kernel, host-planned fd_decode calls: each split publishes its
+    // partial rows by writing `token` (unique per call) into its flag
+    // (flags [Hkv][total_splits], kvh-major), and the last min(G, splits)
+    // CTAs of a group to arrive merge one or more of its heads each.  Null
+    // under the device-side plan: there the group's last CTA merges all heads.
+    int *flags;
+    int32_t token;
     // Persistent grid: items past the first wave are claimed from `claim`;
     // every CTA adds one to `done` when it stops claiming, and the CTA that
     // completes `done` resets both (zero-initialised, in the workspace header).

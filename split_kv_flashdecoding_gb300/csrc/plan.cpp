@@ -210,10 +210,10 @@ extern "C" int fd_plan(int batch, int num_qo_heads, int num_kv_heads, int head_d
     info->ctas_per_sm = ctas_per_sm;
     info->total_tokens = total;
     // fd_decode workspace: status header, one merge ticket per (request, KV
-    // head), partial LSE, partial O.
+    // head), partial LSE, partial O, one publication flag per split item.
     info->workspace_bytes = FD_WORKSPACE_HEADER_BYTES +
                             round_up((int64_t)batch * num_kv_heads * 4, 256) +
-                            round_up(rows * 4, 256) + rows * head_dim * 4;
+                            round_up(rows * 4, 256) + rows * head_dim * 4 + round_up(num_work * 4, 256);
     info->timeout_ns = FD_DEFAULT_TIMEOUT_NS;
     return FD_OK;
 }

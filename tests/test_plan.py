@@ -119,8 +119,10 @@ def test_workspace_bytes():
     info = fd.plan(3, 16, 4, 128, [0, 10, 10, 300], num_sms=10, chunk=64)
     rows = info.num_partial_rows
     group = -(-3 * 4 * 4 // 256) * 256             # one int32 per (request, KV head)
-    # header | merge tickets | partial LSE | partial O
-    assert info.workspace_bytes == 256 + group + -(-rows * 4 // 256) * 256 + rows * 128 * 4
+    flags = -(-info.num_work * 4 // 256) * 256      # one int32 per split item
+    # header | merge tickets | partial LSE | partial O | publication flags
+    assert info.workspace_bytes == (256 + group + -(-rows * 4 // 256) * 256 + rows * 128 * 4 +
+                                    flags)
 
 
 def _makespan(info, ip, slots, overhead=3):
