@@ -471,7 +471,12 @@ def build_case(w, args, dev, rank, fd):
     # when some request has no keys
     any_empty = bool(np.any(np.diff(ip_host) == 0))
     launches_per_step = int(info0.num_work > 0) + int(any_empty)
-    return dict(w=w, inp=inp, ip_host=ip_host, ip_dev=ip_dev, bufs=bufs, copies=copies,
+    # every device buffer the marshalled arguments point at stays referenced
+    # here for as long as the case lives
+    here = dict(locals())
+    keep = [here[n] for n in ("k_scale_dev", "v_scale_dev", "pg_ip_dev", "pg_last_dev", "pg_idx_dev",
+                              "ws_split", "po", "pl", "ws_g") if here.get(n) is not None]
+    return dict(w=w, inp=inp, ip_host=ip_host, ip_dev=ip_dev, bufs=bufs, copies=copies, keep=keep,
                 info=info0, nb=nb, o=o, lse=lse, ws=ws, stream=stream, step=step, split=split,
                 step_name=step_name, step_calls=step_calls, kernel=kernel,
                 launches_per_step=launches_per_step, paged=paged, fp8=fp8, int4=int4, T=T)
@@ -540,19 +545,30 @@ def measure_case(case, args, world, dev, flush, clocks=None, n_flushed=100) -> d
         torch.cuda.synchronize(dev)
         split_ms = ev0.elapsed_time(ev1) / n_split
 
-    # The same step timed one at a time after an L2 flush (includes each
-    # step's launch latency and about 2 us of event overhead).
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_flushed)]
-    for i in range(n_flushed):
-        flush.fill_(float(i))
-        evs[i][0].record(stream)
-        step(0)
-        evs[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    flushed_ms = np.array([a.elapsed_time(b) for a, b in evs]) / calls
+    # The same step timed one at a time (each includes its launch latency and
+    # about 2 us of event overhead) after two kinds of L2 flush: writing a
+    # 1 GiB buffer (L2 left full of dirty lines, whose write-back to HBM then
+    # shares the step's DRAM time), and reading one (L2 full of clean lines of
+    # other data, as after a kernel that mostly reads, e.g. a GEMM).
+    def single_steps(flush_op):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_flushed)]
+        for i in range(n_flushed):
+            flush_op(i)
+            evs[i][0].record(stream)
+            step(0)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return np.array([a.elapsed_time(b) for a, b in evs]) / calls
+
+    flushed_ms = single_steps(lambda i: flush.fill_(float(i)))
+    clean_ms = single_steps(lambda i: flush.sum())
+    status = fd.get_device_status(case["ws"])
+    if status != 0:
+        raise RuntimeError(f"device status {fd.status_string(status)} in the single steps")
     return dict(K=K, rounds=rounds, ms=ms, timed_ms=timed_ms, wall_s=t_wall, split_ms=split_ms,
-                flushed_ms=flushed_ms, launches=rounds * K * case["launches_per_step"])
+                flushed_ms=flushed_ms, clean_ms=clean_ms,
+                launches=rounds * K * case["launches_per_step"])
 
 
 def workload_summary(case, m, world, peak) -> dict:
@@ -566,6 +582,7 @@ def workload_summary(case, m, world, peak) -> dict:
         "frac_of_nominal_8tbs": round(gbs / world / NOMINAL_HBM_GBS, 4),
         "split_only_us": None if m["split_ms"] is None else round(m["split_ms"] * 1e3, 2),
         "step_us_after_l2_flush_p50": round(float(np.percentile(m["flushed_ms"], 50)) * 1e3, 2),
+        "step_us_after_l2_read_flush_p50": round(float(np.percentile(m["clean_ms"], 50)) * 1e3, 2),
         "timed_steps": m["rounds"] * m["K"],
         "timed_region_ms": round(m["timed_ms"], 1),
         "algorithmic_bytes_per_step": nb["step"],
@@ -701,6 +718,12 @@ def run_fd(args, world, rank, local) -> dict | None:
                    "split_only_us": summary["split_only_us"],
                    "step_us_after_l2_flush_p10_p50_p90": [
                        round(float(np.percentile(m["flushed_ms"], p)) * 1e3, 2) for p in (10, 50, 90)],
+                   "step_us_after_l2_read_flush_p10_p50_p90": [
+                       round(float(np.percentile(m["clean_ms"], p)) * 1e3, 2) for p in (10, 50, 90)],
+                   "single_step_note": ("one step at a time after a 1 GiB L2 flush, launch latency and "
+                                        "events included: a write flush leaves L2 full of dirty lines "
+                                        "whose write-back shares the step's DRAM time; a read flush "
+                                        "leaves it full of clean lines of other data"),
                    "wall_s": round(m["wall_s"], 3),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "kv_layout": (f"paged, page_size {args.page_size}, pages scattered in a pool"
