@@ -264,18 +264,30 @@ __device__ __forceinline__ float bf16_round(float x)
 }
 
 // Eight 4-bit two's-complement values (nibble j of each 16-bit half of x; the
-// low nibble first) -> four bf16x2: r[j] = (nibble j of the low half, nibble j
-// of the high half).  Flipping a code's sign bit gives u = n + 8 in 0..15; the
-// bf16 with bits 0x4300 | u is 128 + u (at 128 the unit in the last place is
-// 1), and subtracting 136 leaves n.  Both steps are exact.
-__device__ __forceinline__ void int4x8_to_bf16x2x4(uint32_t x, uint32_t (&r)[4])
+// low nibble first) -> four f16x2: r[j] = (nibble j of the low half, nibble j
+// of the high half).  Per half, the nibbles at bits 0-3 and 4-7 are taken in
+// place: one lop3 keeps the nibble, flips its sign bit (u = n + 8) and sets
+// the exponent of 1024, which gives the f16 1024 + u (bits 0-3, where the unit
+// in the last place is 1) or 1024 + 16 u (bits 4-7); subtracting 1032, or a
+// multiply-add by 1/16 and -72, leaves n.  Nibbles 2 and 3 do the same after
+// one shift by 8.  Every step is exact.
+__device__ __forceinline__ void int4x8_to_f16x2x4(uint32_t x, uint32_t (&r)[4])
 {
-    constexpr uint32_t kMagic = 0x43084308u;   // (0x4300 | 8) in both halves: 136.0
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t t = ((x >> (4 * j)) & 0x000F000Fu) ^ kMagic;
-        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r[j]) : "r"(t), "r"(kMagic));
-    }
+    // lop3 0x6A = (b & (a ^ c)) | (~b & c): a nibble of a under mask b with
+    // its sign bit flipped by c, and c's exponent bits elsewhere
+    auto pick = [](uint32_t a, uint32_t mask, uint32_t c) {
+        uint32_t d;
+        asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(mask), "r"(c));
+        return d;
+    };
+    const uint32_t y = x >> 8;
+    const uint32_t t0 = pick(x, 0x000F000Fu, 0x64086408u), t1 = pick(x, 0x00F000F0u, 0x64806480u);
+    const uint32_t t2 = pick(y, 0x000F000Fu, 0x64086408u), t3 = pick(y, 0x00F000F0u, 0x64806480u);
+    constexpr uint32_t k1032 = 0x64086408u, kSixteenth = 0x2C002C00u, kMinus72 = 0xD480D480u;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(k1032));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[1]) : "r"(t1), "r"(kSixteenth), "r"(kMinus72));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r[2]) : "r"(t2), "r"(k1032));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[3]) : "r"(t3), "r"(kSixteenth), "r"(kMinus72));
 }
 
 // 16 zero bytes to shared memory (32-bit shared address, 16-byte aligned).
@@ -431,7 +443,7 @@ __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, in
 //    same order.  For P V, ldmatrix.trans gives lane (g, t4) dims 16c + 2g and
 //    +1 of keys 2t4 and 2t4+1, so one tile of columns takes the even dims and
 //    one the odd: o_acc[2c + e] holds dims 16c + 4t4 + e (and + 2).
-//  INT4: mma.sync bf16; the four-bit codes are widened to bf16 (exact) in
+//  INT4: mma.sync f16; the four-bit codes are widened to f16 (exact) in
 //    registers.  An ldmatrix of the 64-byte key rows gives lane (g, t4) dims
 //    32c + 8t4 .. +7 of key g in one word; nibbles j and j + 4 pair up, so
 //    k-step 2c + h takes dims 32c + 8t4 + 2h (+4) at k 2t4 (+1) and + 2h + 1
@@ -483,9 +495,9 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t b[4];   // b[j]: dims 32c + 8t4 + j and + 4 of key 8 jn + g
-                int4x8_to_bf16x2x4(kb[c], b);
-                mma_bf16(sc[jn], qa[2 * c][0], 0u, qa[2 * c][1], 0u, b[0], b[1]);
-                mma_bf16(sc[jn], qa[2 * c + 1][0], 0u, qa[2 * c + 1][1], 0u, b[2], b[3]);
+                int4x8_to_f16x2x4(kb[c], b);
+                mma_f16(sc[jn], qa[2 * c][0], 0u, qa[2 * c][1], 0u, b[0], b[1]);
+                mma_f16(sc[jn], qa[2 * c + 1][0], 0u, qa[2 * c + 1][1], 0u, b[2], b[3]);
             }
         }
     } else if constexpr (S::kFp8) {
@@ -575,7 +587,7 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
             p2 = k0 + 8 < n_valid ? p2 * lds_f32(vk + 32) : 0.f;
             p3 = k0 + 9 < n_valid ? p3 * lds_f32(vk + 36) : 0.f;
         }
-        if constexpr (S::kFp8) {
+        if constexpr (S::kFp8 || S::kInt4) {
             const float h0 = f16_round(p0), h1 = f16_round(p1);
             const float h2 = f16_round(p2), h3 = f16_round(p3);
             pa[ks][0] = pack_f16(h0, h1);
@@ -607,12 +619,12 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
                 for (int h = 0; h < 2; ++h) {         // chunk c = 2 cp + h: vb[2h] keys +0..7, vb[2h+1] +8..15
                     const int c = 2 * cp + h;
                     uint32_t lo[4], hi[4];            // [j]: dim 32c + 4g + j of keys 2t4, 2t4 + 1
-                    int4x8_to_bf16x2x4(vb[2 * h], lo);
-                    int4x8_to_bf16x2x4(vb[2 * h + 1], hi);
+                    int4x8_to_f16x2x4(vb[2 * h], lo);
+                    int4x8_to_f16x2x4(vb[2 * h + 1], hi);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        mma_bf16(o_acc[4 * c + j], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], lo[j],
-                                 hi[j]);
+                        mma_f16(o_acc[4 * c + j], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], lo[j],
+                                hi[j]);
                 }
             }
         }
@@ -862,8 +874,9 @@ __device__ __forceinline__ KeyIndex key_index(const SplitParams &p, bool paged)
 //    that puts its largest magnitude in [2^8, 2^9), so every bf16 value of the
 //    row converts to f16 exactly (values below 2^-22 of the row's maximum
 //    round in f16's subnormal range); returns the inverse power.
-//  INT4 (bf16 MMA): qa[2c + h] = dims 32c + 8t4 + 2h (+4) and 32c + 8t4 + 2h + 1
-//    (+4), the order consume_tile reads K in; 1.
+//  INT4 (f16 MMA): qa[2c + h] = dims 32c + 8t4 + 2h (+4) and 32c + 8t4 + 2h + 1
+//    (+4), the order consume_tile reads K in, each row scaled into f16 as for
+//    FP8; returns the inverse power.
 template <int G, int DT, bool GLOBAL>
 __device__ __forceinline__ float load_q(const uint16_t *qrows, int lane, uint32_t (&qa)[8][2])
 {
@@ -871,22 +884,46 @@ __device__ __forceinline__ float load_q(const uint16_t *qrows, int lane, uint32_
     const bool valid = g_row < G;
     if constexpr (DT == kKvInt4) {
         const uint4 *row = reinterpret_cast<const uint4 *>(qrows + (valid ? g_row : 0) * kHeadDim);
+        uint4 raw[4];
+        float amax = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            uint4 raw = make_uint4(0u, 0u, 0u, 0u);   // dims 32c + 8t4 .. +7
+            raw[c] = make_uint4(0u, 0u, 0u, 0u);   // dims 32c + 8t4 .. +7
             if constexpr (GLOBAL) {
                 if (valid)
-                    raw = __ldg(row + 4 * c + t4);
+                    raw[c] = __ldg(row + 4 * c + t4);
             } else {
                 if (valid)
-                    raw = row[4 * c + t4];
+                    raw[c] = row[4 * c + t4];
             }
-            qa[2 * c][0] = __byte_perm(raw.x, raw.z, 0x5410);       // dims +0, +4
-            qa[2 * c][1] = __byte_perm(raw.x, raw.z, 0x7632);       // dims +1, +5
-            qa[2 * c + 1][0] = __byte_perm(raw.y, raw.w, 0x5410);   // dims +2, +6
-            qa[2 * c + 1][1] = __byte_perm(raw.y, raw.w, 0x7632);   // dims +3, +7
+            const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 a = bf16x2_to_float2(w[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(a.x), fabsf(a.y)));
+            }
         }
-        return 1.f;
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int sh = 0;
+        if (amax > 0.f) {
+            int e;
+            frexpf(amax, &e);
+            sh = min(max(9 - e, -100), 100);
+        }
+        const float up = __int_as_float((127 + sh) << 23);
+        auto f16pair = [&](uint32_t pair) {   // a bf16x2 pair -> f16x2, times 2^sh (exact)
+            const float2 a = bf16x2_to_float2(pair);
+            return pack_f16(a.x * up, a.y * up);
+        };
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            qa[2 * c][0] = f16pair(__byte_perm(raw[c].x, raw[c].z, 0x5410));       // dims +0, +4
+            qa[2 * c][1] = f16pair(__byte_perm(raw[c].x, raw[c].z, 0x7632));       // dims +1, +5
+            qa[2 * c + 1][0] = f16pair(__byte_perm(raw[c].y, raw[c].w, 0x5410));   // dims +2, +6
+            qa[2 * c + 1][1] = f16pair(__byte_perm(raw[c].y, raw[c].w, 0x7632));   // dims +3, +7
+        }
+        return __int_as_float((127 - sh) << 23);
     } else if constexpr (DT == kKvFp8) {
         const uint2 *row = reinterpret_cast<const uint2 *>(qrows + (valid ? g_row : 0) * kHeadDim);
         uint2 raw[8];
