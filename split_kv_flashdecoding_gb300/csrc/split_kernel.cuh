@@ -1267,12 +1267,23 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                                 prefetch_box<SG>(&tm_k, &tm_v, kvh, c.base + t0p + i * kTile);
                     } else if (c.base >= 0 && c.base + c.pages <= p.num_page_entries) {
                         constexpr int kBox = SG::kBoxRows;
+                        // boxes per lane: all of a lane's page ids are loaded
+                        // before its first prefetch, so one L2 round trip (not
+                        // one per box) delays the early launch
+                        constexpr int kPerLane = (kPrefetchTiles * (kTile / kBox) + 31) / 32;
                         const int32_t t_end = min(t1p, t0p + kPrefetchTiles * kTile);
-                        for (int32_t t = t0p + lane * kBox; t < t_end; t += 32 * kBox) {
+                        int32_t ids[kPerLane];
+#pragma unroll
+                        for (int j = 0; j < kPerLane; ++j) {
+                            const int32_t t = t0p + (lane + 32 * j) * kBox;
                             const int32_t pg = t / p.page_size;
-                            const int32_t id = pg < c.pages ? __ldcg(p.page_indices + c.base + pg) : -1;
-                            if (id >= 0 && id < p.num_pages)
-                                prefetch_box<SG>(&tm_k, &tm_v, kvh, id * p.page_size + t % p.page_size);
+                            ids[j] = t < t_end && pg < c.pages ? __ldcg(p.page_indices + c.base + pg) : -1;
+                        }
+#pragma unroll
+                        for (int j = 0; j < kPerLane; ++j) {
+                            const int32_t t = t0p + (lane + 32 * j) * kBox;
+                            if (ids[j] >= 0 && ids[j] < p.num_pages)
+                                prefetch_box<SG>(&tm_k, &tm_v, kvh, ids[j] * p.page_size + t % p.page_size);
                         }
                     }
                     __syncwarp();
