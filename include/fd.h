@@ -305,12 +305,11 @@ int fd_decode_paged_fp8(int batch, int num_qo_heads, int num_kv_heads, int head_
  * the dequantised K and V (the codes widen to f16 exactly and each q row is
  * scaled into f16 by a power of two, as for FP8; each row's K scale multiplies
  * its logit in fp32, and its V scale its softmax weight, which enters P V as
- * an f16 hi + lo pair).  So |v_scale| must stay below 65504, the largest f16
- * (a weight times a larger scale overflows); a weight times a scale below
- * 2^-14 keeps an absolute accuracy of 2^-25.  A scale of +-inf or NaN
- * propagates; the scales of rows past a request's last key (the rest of its
- * last page) are never used.  Workspace and plan as for fd_decode /
- * fd_decode_paged.
+ * an f16 hi + lo pair after division by a power of two that bounds the V
+ * scales seen so far, so scales of any finite magnitude keep the path's
+ * relative accuracy).  A scale of +-inf or NaN propagates (as NaN); the scales
+ * of rows past a request's last key (the rest of its last page) are never
+ * used.  Workspace and plan as for fd_decode / fd_decode_paged.
  */
 int fd_decode_int4(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                    const int32_t *kv_indptr_host, const int32_t *kv_indptr_dev,

@@ -111,6 +111,13 @@ struct Stage {
     }
 };
 constexpr int kMaxGroup = 8;                   // rows 8-15 of the MMA carry the lo part of P
+constexpr int kNoExp = -1000;                  // INT4 V-scale exponent before any nonzero scale
+
+// 2^k as a float, exactly, for k in [-126, 127]; 0 below, +inf above.
+__device__ __forceinline__ float pow2i(int k)
+{
+    return k < -126 ? 0.f : k > 127 ? INFINITY : __int_as_float((127 + k) << 23);
+}
 
 enum Misc { kAbort, kIssued, kDescs, kLast, kFinalK, kMiscCount };
 
@@ -455,7 +462,7 @@ __device__ __forceinline__ void merge_group(const SplitParams &p, int prefix, in
 template <int KV, int DT>
 __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uint32_t (&qa)[8][2],
                                              float qk_scale, int lane, float &m_run, float &l_part,
-                                             float (&o_acc)[16][4])
+                                             float (&o_acc)[16][4], int &v_exp)
 {
     using S = Stage<KV, DT>;
     const int t4 = lane & 3;
@@ -561,31 +568,64 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int n_valid, const uin
         psum += x[e];
     }
     l_part = fmaf(l_part, alpha, psum);
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+    // INT4: the tile's V scales (0 for masked keys: another request's row or
+    // past the end is never read).  P V runs in f16, so the weights enter it as
+    // p * v_scale * 2^-v_exp, where 2^v_exp bounds every V scale seen so far
+    // by this warp: the products stay in [-1, 1], far from f16's overflow and
+    // subnormal range, whatever the scales.  When v_exp grows, O is rescaled
+    // by the same exact power of two, together with the softmax rescale;
+    // write_state multiplies 2^v_exp back.
+    float vs[2][4] = {};
+    float oscale = alpha;
+    if constexpr (S::kInt4) {
+        float vmax = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int k0 = 16 * ks + 2 * t4;   // keys k0 (+1) and k0 + 8 (+9)
+            const uint32_t vk = vs_base + 4 * k0;
+            vs[ks][0] = k0 < n_valid ? lds_f32(vk) : 0.f;
+            vs[ks][1] = k0 + 1 < n_valid ? lds_f32(vk + 4) : 0.f;
+            vs[ks][2] = k0 + 8 < n_valid ? lds_f32(vk + 32) : 0.f;
+            vs[ks][3] = k0 + 9 < n_valid ? lds_f32(vk + 36) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                vmax = fmaxf(vmax, fabsf(vs[ks][j]));
+        }
+        // lanes of one t4 hold the same keys: the warp's 32 keys in 2 steps
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+        if (!(vmax <= 0.f)) {   // a nonzero, inf or NaN scale: vmax < 2^e
+            const int e = ((__float_as_int(vmax) >> 23) & 0xFF) - 126;
+            if (e > v_exp) {
+                oscale *= pow2i(v_exp - e);   // 0 when v_exp is still kNoExp
+                v_exp = e;
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, oscale != 1.f)) {
 #pragma unroll
         for (int n = 0; n < 16; ++n) {
-            o_acc[n][0] *= alpha;
-            o_acc[n][1] *= alpha;
-            o_acc[n][2] *= alpha;
-            o_acc[n][3] *= alpha;
+            o_acc[n][0] *= oscale;
+            o_acc[n][1] *= oscale;
+            o_acc[n][2] *= oscale;
+            o_acc[n][3] *= oscale;
         }
     }
     // P as the A operand: k-step ks covers keys 16ks .. 16ks+15 (n-tiles
     // 2ks, 2ks+1); rows 0-7 hi, rows 8-15 lo = P - hi, in the MMA's type.
     uint32_t pa[2][4];
+    // INT4: 2^-v_exp (NaN-propagating 0 once an infinite or NaN scale was seen)
+    const float vinv = S::kInt4 ? (v_exp == kNoExp ? 1.f : pow2i(-v_exp)) : 1.f;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         float p0 = x[4 * ks], p1 = x[4 * ks + 1];
         float p2 = x[4 * ks + 2], p3 = x[4 * ks + 3];
         if constexpr (S::kInt4) {
-            // keys 16ks + 2t4 (+1) and 16ks + 8 + 2t4 (+1); a masked key's
-            // scale (another request's row, or past the end) is not read
-            const int k0 = 16 * ks + 2 * t4;
-            const uint32_t vk = vs_base + 4 * k0;
-            p0 = k0 < n_valid ? p0 * lds_f32(vk) : 0.f;
-            p1 = k0 + 1 < n_valid ? p1 * lds_f32(vk + 4) : 0.f;
-            p2 = k0 + 8 < n_valid ? p2 * lds_f32(vk + 32) : 0.f;
-            p3 = k0 + 9 < n_valid ? p3 * lds_f32(vk + 36) : 0.f;
+            // keys 16ks + 2t4 (+1) and 16ks + 8 + 2t4 (+1)
+            p0 *= vs[ks][0] * vinv;
+            p1 *= vs[ks][1] * vinv;
+            p2 *= vs[ks][2] * vinv;
+            p3 *= vs[ks][3] * vinv;
         }
         if constexpr (S::kFp8 || S::kInt4) {
             const float h0 = f16_round(p0), h1 = f16_round(p1);
@@ -992,11 +1032,11 @@ __device__ __forceinline__ void write_state(uint8_t *state, int warp, int lane,
             for (int c = 0; c < 4; ++c) {   // dims 32c + 8t4 + (0..3), then + (4..7)
                 const int n = 4 * c;
                 *reinterpret_cast<float4 *>(dst + 32 * c) = make_float4(
-                    o_acc[n][0] + o_acc[n][2], o_acc[n + 1][0] + o_acc[n + 1][2],
-                    o_acc[n + 2][0] + o_acc[n + 2][2], o_acc[n + 3][0] + o_acc[n + 3][2]);
+                    (o_acc[n][0] + o_acc[n][2]) * vscale, (o_acc[n + 1][0] + o_acc[n + 1][2]) * vscale,
+                    (o_acc[n + 2][0] + o_acc[n + 2][2]) * vscale, (o_acc[n + 3][0] + o_acc[n + 3][2]) * vscale);
                 *reinterpret_cast<float4 *>(dst + 32 * c + 4) = make_float4(
-                    o_acc[n][1] + o_acc[n][3], o_acc[n + 1][1] + o_acc[n + 1][3],
-                    o_acc[n + 2][1] + o_acc[n + 2][3], o_acc[n + 3][1] + o_acc[n + 3][3]);
+                    (o_acc[n][1] + o_acc[n][3]) * vscale, (o_acc[n + 1][1] + o_acc[n + 1][3]) * vscale,
+                    (o_acc[n + 2][1] + o_acc[n + 2][3]) * vscale, (o_acc[n + 3][1] + o_acc[n + 3][3]) * vscale);
             }
         } else if constexpr (DT == kKvFp8) {
             float *dst = comb_acc + (warp * G + g_row) * kHeadDim + 4 * t4;
@@ -1212,6 +1252,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         griddep_wait();
 
     float m_run = -INFINITY, l_part = 0.f, vscale = 1.f;
+    int v_exp = kNoExp;   // INT4: see consume_tile
     float o_acc[16][4];
 #pragma unroll
     for (int n = 0; n < 16; ++n)
@@ -1455,7 +1496,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                     break;
                 }
                 consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc);
+                                     qk, lane, m_run, l_part, o_acc, v_exp);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1493,6 +1534,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     int ticket = 0;
     if (spread && tid == 0)
         ticket = atomicAdd(p.counters + (int64_t)it.b * p.num_kv_heads + it.kvh, 1);
+    if constexpr (DT == kKvInt4)
+        vscale = v_exp == kNoExp ? 1.f : pow2i(v_exp);
     if (warp < NC)
         write_state<G, NC, DT>(smem, warp, lane, o_acc, m_run, l_part, vscale);
     __syncthreads();
@@ -1736,6 +1779,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
         while (ok && it.state == kItemOk) {
             const int slot = k % kDescSlots;
             float m_run = -INFINITY, l_part = 0.f;
+            int v_exp = kNoExp;   // INT4: see consume_tile
             float o_acc[16][4];
 #pragma unroll
             for (int n = 0; n < 16; ++n)
@@ -1758,7 +1802,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                     break;
                 }
                 consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc);
+                                     qk, lane, m_run, l_part, o_acc, v_exp);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1784,7 +1828,8 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                 break;
             }
             write_state<G, NC, DT>(states + sb * L::kStateBytes, warp, lane, o_acc, m_run, l_part,
-                                   __int_as_float(it.vs));
+                                   DT == kKvInt4 ? (v_exp == kNoExp ? 1.f : pow2i(v_exp))
+                                                 : __int_as_float(it.vs));
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&state_full[sb]));

@@ -147,3 +147,32 @@ def test_int4_rejects_misaligned_scales(cuda_device):
                                  P(d["v_scale_int4"].data_ptr()), float(f["scale"]), P(o.data_ptr()),
                                  P(lse.data_ptr()), P(ws.data_ptr()), ws.numel(), None)
     assert rc == -1
+
+
+@pytest.mark.parametrize("regime", ["tiny", "huge", "log_spread"])
+def test_int4_v_scales_of_any_magnitude(cuda_device, regime):
+    """P V runs on f16 tensor cores with the weights p * v_scale brought into
+    [-1, 1] by a running power of two per warp, so V scales far below f16's
+    normal range (1e-9) or far above its largest value (1e9), or spread over
+    thirteen decades within a request, keep the path's relative accuracy:
+    compared with the oracle relative to the output's own magnitude."""
+    f = random_int4(make_small(3, 32, 8, 128, [2000, 333, 4096], seed=71), seed=72)
+    g = torch.Generator().manual_seed(73)
+    T = f["v_scale_int4"].shape[1]
+    sign = torch.where(torch.rand(8, T, generator=g) < 0.5, -1.0, 1.0)
+    if regime == "tiny":
+        mag = 1e-9 * (1 + torch.rand(8, T, generator=g))
+    elif regime == "huge":
+        mag = 1e9 * (1 + torch.rand(8, T, generator=g))
+    else:
+        mag = 10.0 ** (torch.rand(8, T, generator=g) * 13 - 9)   # 1e-9 .. 1e4
+    f["v_scale_int4"] = (sign * mag).float()
+    o, lse = _run(f, cuda_device)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = _ref(f)
+    o_h = o.reshape(o_ref.shape).cpu().double().numpy()
+    scale = np.abs(o_ref).max()
+    assert np.isfinite(o_h).all()
+    assert np.abs(o_h - o_ref).max() <= 1e-4 * scale, regime
+    assert np.linalg.norm(o_h - o_ref) <= 1e-5 * np.linalg.norm(o_ref), regime
+    assert np.abs(lse.reshape(-1).cpu().numpy() - lse_ref).max() <= 2e-5
