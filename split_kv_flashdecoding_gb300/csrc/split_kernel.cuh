@@ -211,6 +211,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
                  : "r"(addr));
 }
 
+// The warp's 8x8 matrix of 16-bit elements (lane (g, t4) holds row g,
+// columns 2t4 and 2t4 + 1) transposed, in the same fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // D (+)= A B for one m16n8k16 tile, bf16 inputs, fp32 accumulator.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1)
@@ -908,6 +917,8 @@ __device__ __forceinline__ KeyIndex key_index(const SplitParams &p, bool paged)
 // Q fragments (A operand of S = Q K^T) for the 8 k-steps of 16 dims from the
 // G bf16 query rows at `qrows` (global or shared); rows g >= G and the padding
 // rows 8-15 are zero.  Returns the factor the logits must be multiplied by.
+// COLS: the same registers as the B operand of S^T = K Q^T, column g holding
+// query row g mod G (every column filled).
 //  bf16: qa[c] = dims 16c + 2t4 (+1) and 16c + 8 + 2t4 (+1), as stored; 1.
 //  FP8 (f16 MMA): qa[c] = dims 16c + 4t4 (+1) and 16c + 4t4 + 2 (+3), the order
 //    consume_tile reads K in.  Each row is first scaled by the power of two
@@ -917,11 +928,11 @@ __device__ __forceinline__ KeyIndex key_index(const SplitParams &p, bool paged)
 //  INT4 (f16 MMA): qa[2c + h] = dims 32c + 8t4 + 2h (+4) and 32c + 8t4 + 2h + 1
 //    (+4), the order consume_tile reads K in, each row scaled into f16 as for
 //    FP8; returns the inverse power.
-template <int G, int DT, bool GLOBAL>
+template <int G, int DT, bool GLOBAL, bool COLS = false>
 __device__ __forceinline__ float load_q(const uint16_t *qrows, int lane, uint32_t (&qa)[8][2])
 {
-    const int g_row = lane >> 2, t4 = lane & 3;
-    const bool valid = g_row < G;
+    const int g_row = COLS ? (lane >> 2) & (G - 1) : lane >> 2, t4 = lane & 3;
+    const bool valid = COLS || g_row < G;
     if constexpr (DT == kKvInt4) {
         const uint4 *row = reinterpret_cast<const uint4 *>(qrows + (valid ? g_row : 0) * kHeadDim);
         uint4 raw[4];
@@ -1061,6 +1072,275 @@ __device__ __forceinline__ void write_state(uint8_t *state, int warp, int lane,
     }
 }
 
+// A consumer warp's online-softmax state for one item in the row form
+// (S = Q K^T, the query rows in the MMA's rows; every K/V type and group
+// size): begin() resets it with the logit factor of the lane's query row,
+// tile() takes one stage, write() hands the state to the CTA's combine.
+template <int G, int KV, int DT>
+struct RowConsumer {
+    float o_acc[16][4];
+    float m_run, l_part, qk;
+    int v_exp;   // INT4: see consume_tile
+
+    __device__ __forceinline__ void begin(float qk_row, int)
+    {
+        qk = qk_row;
+        m_run = -INFINITY;
+        l_part = 0.f;
+        v_exp = kNoExp;
+#pragma unroll
+        for (int n = 0; n < 16; ++n)
+            o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+    }
+    __device__ __forceinline__ void tile(uint32_t st, int n_valid, const uint32_t (&qa)[8][2], int lane)
+    {
+        consume_tile<KV, DT>(st, n_valid, qa, qk, lane, m_run, l_part, o_acc, v_exp);
+    }
+    // fp8_vscale: the head's V scale (FP8 K/V; ignored otherwise)
+    template <int NC>
+    __device__ __forceinline__ void write(uint8_t *state, int warp, int lane, float fp8_vscale) const
+    {
+        const float vscale = DT == kKvInt4 ? (v_exp == kNoExp ? 1.f : pow2i(v_exp)) : fp8_vscale;
+        write_state<G, NC, DT>(state, warp, lane, o_acc, m_run, l_part, vscale);
+    }
+};
+
+// The column form for INT4 K/V and G <= 4: S^T = K Q^T and O^T = V^T P^T, the
+// tile's keys (scores) and the head's dims (output) in the MMA's 16 rows and
+// the query heads in its 8 columns, so every MMA row carries data: half the
+// MMAs and half the output accumulators of the row form, whose padding rows
+// 8-15 carry nothing in Q K^T.  Column n < G is head n with the hi part of
+// its P V weights, column G + n the same head with the lo part (the f16
+// weights keep about 22 bits, as in the row form), columns >= 2G repeat
+// heads and are dropped.  Q fills every column (load_q<..., COLS>), so a lo
+// column computes the same scores, maxima and sums as its hi column in its
+// own lanes and needs no exchange until write().
+//  Lane (g, t4) holds scores of keys g, g + 8, 16 + g, 24 + g for columns
+//  2t4 and 2t4 + 1 (m[e], l[e], qk[e]: column 2t4 + e).  P^T as the B operand
+//  is the transpose of the score fragments (movmatrix).  o[2c + jp] holds
+//  dims 32c + 4g + 2jp (c0, c1) and + 1 (c2, c3) for the lane's two columns.
+template <int G, int KV>
+struct ColumnConsumer {
+    static_assert(G == 1 || G == 2 || G == 4, "column form: two columns per head");
+    float o[8][4];
+    float m[2], l[2], qk[2], lo[2];
+    int v_exp;
+
+    __device__ __forceinline__ void begin(float qk_row, int lane)
+    {
+        const int t4 = lane & 3;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = 2 * t4 + e;   // this lane's column: head n mod G, from lane 4 (n mod G)
+            qk[e] = __shfl_sync(0xffffffffu, qk_row, (n & (G - 1)) * 4);
+            lo[e] = n >= G && n < 2 * G ? 1.f : 0.f;
+            m[e] = -INFINITY;
+            l[e] = 0.f;
+        }
+        v_exp = kNoExp;
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+            o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    }
+
+    __device__ __forceinline__ void tile(uint32_t st, int n_valid, const uint32_t (&qa)[8][2], int lane)
+    {
+        using S = Stage<KV, kKvInt4>;
+        const int g = lane >> 2, lr = lane & 7, lm = lane >> 3;
+
+        // ---- S^T = K Q^T: m-block mb = keys 16 mb + g (rows g), 16 mb + 8 + g
+        // (rows g + 8).  ldmatrix gives lane (g, t4) the codes of dims
+        // 32c + 8t4 .. +7 of a key in word c; widened, k-step 2c + h takes
+        // dims + 2h (+4) at k 2t4 (+1) and + 2h + 1 (+4) at k 2t4 + 8 (+9), the
+        // order load_q puts Q in.
+        float s[2][4];
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+            s[mb][0] = s[mb][1] = s[mb][2] = s[mb][3] = 0.f;
+            uint32_t k0[4], k1[4];
+            const int r0 = 16 * mb + lr, r1 = r0 + 8;
+            ldsm_x4(st + r0 * 64 + ((lm ^ ((r0 >> 1) & 3)) << 4), k0);
+            ldsm_x4(st + r1 * 64 + ((lm ^ ((r1 >> 1) & 3)) << 4), k1);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t a[4], b[4];   // [j]: dims 32c + 8t4 + j and + 4 of keys 16mb + g, + 8
+                int4x8_to_f16x2x4(k0[c], a);
+                int4x8_to_f16x2x4(k1[c], b);
+                mma_f16(s[mb], a[0], b[0], a[1], b[1], qa[2 * c][0], qa[2 * c][1]);
+                mma_f16(s[mb], a[2], b[2], a[3], b[3], qa[2 * c + 1][0], qa[2 * c + 1][1]);
+            }
+        }
+
+        // ---- online softmax per column over the warp's 32 keys (the 8 lanes
+        // of a t4 hold them: reductions over g), with the K and V scales of
+        // the lane's 4 keys; the V exponent as in the row form (consume_tile)
+        const uint32_t ks_base = st + S::kKsOff, vs_base = st + S::kVsOff;
+        float x[2][4], vs[2][2];
+        float mt0 = -INFINITY, mt1 = -INFINITY, vmax = 0.f;
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int key = 16 * mb + 8 * hf + g;
+                const bool ok = key < n_valid;
+                const float ksc = lds_f32(ks_base + 4 * key);
+                const float v0 = ok ? s[mb][2 * hf] * ksc * qk[0] : -INFINITY;
+                const float v1 = ok ? s[mb][2 * hf + 1] * ksc * qk[1] : -INFINITY;
+                x[mb][2 * hf] = v0;
+                x[mb][2 * hf + 1] = v1;
+                mt0 = fmaxf(mt0, v0);
+                mt1 = fmaxf(mt1, v1);
+                vs[mb][hf] = ok ? lds_f32(vs_base + 4 * key) : 0.f;
+                vmax = fmaxf(vmax, fabsf(vs[mb][hf]));
+            }
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, sh));
+            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, sh));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, sh));
+        }
+        const float m0 = fmaxf(m[0], mt0), m1 = fmaxf(m[1], mt1);
+        float os0 = exp2f(m[0] - m0), os1 = exp2f(m[1] - m1);
+        m[0] = m0;
+        m[1] = m1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                x[mb][2 * hf] = exp2f(x[mb][2 * hf] - m0);
+                x[mb][2 * hf + 1] = exp2f(x[mb][2 * hf + 1] - m1);
+                ps0 += x[mb][2 * hf];
+                ps1 += x[mb][2 * hf + 1];
+            }
+        l[0] = fmaf(l[0], os0, ps0);
+        l[1] = fmaf(l[1], os1, ps1);
+        if (!(vmax <= 0.f)) {   // a nonzero, inf or NaN scale: vmax < 2^e
+            const int e = ((__float_as_int(vmax) >> 23) & 0xFF) - 126;
+            if (e > v_exp) {
+                const float f = pow2i(v_exp - e);   // 0 when v_exp is still kNoExp
+                os0 *= f;
+                os1 *= f;
+                v_exp = e;
+            }
+        }
+        if (__any_sync(0xffffffffu, os0 != 1.f || os1 != 1.f)) {
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                o[n][0] *= os0;
+                o[n][1] *= os1;
+                o[n][2] *= os0;
+                o[n][3] *= os1;
+            }
+        }
+
+        // ---- P^T (B operand of k-step mb: keys 16 mb + 2t4 (+1) in b0,
+        // + 8 in b1, column g): the weights p * v_scale * 2^-v_exp as f16 (hi
+        // columns) or their remainder after f16 (lo columns), packed per key
+        // row and transposed
+        const float vinv = v_exp == kNoExp ? 1.f : pow2i(-v_exp);
+        uint32_t pt[2][2];
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float w = vs[mb][hf] * vinv;
+                float p0 = x[mb][2 * hf] * w, p1 = x[mb][2 * hf + 1] * w;
+                p0 = fmaf(-lo[0], f16_round(p0), p0);
+                p1 = fmaf(-lo[1], f16_round(p1), p1);
+                pt[mb][hf] = movmatrix_trans(pack_f16(p0, p1));
+            }
+
+        // ---- O^T += V^T P^T: k-step ks = keys 16 ks .. +15; m-block (c, jp)
+        // = dims 32c + 4g + 2jp (rows g) and + 1 (rows g + 8).  ldmatrix.trans
+        // gives lane (g, t4) dims 32c + 4g .. +3 of keys 2t4 and 2t4 + 1 in one
+        // word, widened to (key 2t4, key 2t4 + 1) pairs per dim.
+        const uint32_t vt = st + S::kTensorBytes;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            // matrix lm: keys 16 ks + 8 (lm & 1) .. +7, chunk 2 cp + (lm >> 1)
+            const int r = 16 * ks + 8 * (lm & 1) + lr;
+#pragma unroll
+            for (int cp = 0; cp < 2; ++cp) {
+                uint32_t vb[4];
+                ldsm_x4_trans(vt + r * 64 + (((2 * cp + (lm >> 1)) ^ ((r >> 1) & 3)) << 4), vb);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {   // chunk c = 2 cp + h
+                    const int c = 2 * cp + h;
+                    uint32_t a[4], b[4];        // [j]: dim 32c + 4g + j of keys 2t4, 2t4 + 1 (+8 in b)
+                    int4x8_to_f16x2x4(vb[2 * h], a);
+                    int4x8_to_f16x2x4(vb[2 * h + 1], b);
+#pragma unroll
+                    for (int jp = 0; jp < 2; ++jp)
+                        mma_f16(o[2 * c + jp], a[2 * jp], a[2 * jp + 1], b[2 * jp], b[2 * jp + 1],
+                                pt[ks][0], pt[ks][1]);
+                }
+            }
+        }
+    }
+
+    // O of head n = hi column n + lo column G + n (lane ^ G/2, or the lane's
+    // other column for G = 1), times 2^v_exp; the row sums summed over g.
+    template <int NC>
+    __device__ __forceinline__ void write(uint8_t *state, int warp, int lane, float) const
+    {
+        float *comb_acc = reinterpret_cast<float *>(state);
+        float *comb_m = comb_acc + NC * G * kHeadDim;
+        float *comb_l = comb_m + NC * G;
+        const int g = lane >> 2, t4 = lane & 3;
+        const float vscale = v_exp == kNoExp ? 1.f : pow2i(v_exp);
+        float lt[2] = {l[0], l[1]};
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            lt[0] += __shfl_xor_sync(0xffffffffu, lt[0], sh);
+            lt[1] += __shfl_xor_sync(0xffffffffu, lt[1], sh);
+        }
+        if constexpr (G == 1) {
+            if (t4 == 0) {
+                float *dst = comb_acc + warp * kHeadDim + 4 * g;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<float4 *>(dst + 32 * c) =
+                        make_float4((o[2 * c][0] + o[2 * c][1]) * vscale, (o[2 * c][2] + o[2 * c][3]) * vscale,
+                                    (o[2 * c + 1][0] + o[2 * c + 1][1]) * vscale,
+                                    (o[2 * c + 1][2] + o[2 * c + 1][3]) * vscale);
+                if (g == 0) {
+                    comb_m[warp] = m[0];
+                    comb_l[warp] = lt[0];
+                }
+            }
+        } else {
+            float tot[8][4];
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    tot[n][i] = o[n][i] + __shfl_xor_sync(0xffffffffu, o[n][i], G / 2);
+            if (t4 < G / 2) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {   // head 2t4 + e
+                    float *dst = comb_acc + (warp * G + 2 * t4 + e) * kHeadDim + 4 * g;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<float4 *>(dst + 32 * c) =
+                            make_float4(tot[2 * c][e] * vscale, tot[2 * c][2 + e] * vscale,
+                                        tot[2 * c + 1][e] * vscale, tot[2 * c + 1][2 + e] * vscale);
+                    if (g == 0) {
+                        comb_m[warp * G + 2 * t4 + e] = m[e];
+                        comb_l[warp * G + 2 * t4 + e] = lt[e];
+                    }
+                }
+            }
+        }
+    }
+};
+
+// INT4 K/V with G <= 4 take the column form.
+template <int G, int DT>
+constexpr bool kColumnForm = DT == kKvInt4 && G <= 4;
+template <int G, int KV, int DT>
+using Consumer = std::conditional_t<kColumnForm<G, DT>, ColumnConsumer<G, KV>, RowConsumer<G, KV, DT>>;
+
 // Combine the NC consumer states in `state` (NW warps, thread `tid` of
 // NW * 32) into the item's normalised partial rows, or, when `direct`, into
 // the request's O / LSE rows (stage 2 fused and the request has one split).
@@ -1154,7 +1434,7 @@ __device__ __forceinline__ void finish_item(const SplitParams &p, const Item &it
 // Stage 2 is spread over the group's last min(G, splits) CTAs to arrive, one
 // or more heads each, so that no single SM pulls the whole group's partials
 // from L2: `ticket` is this CTA's arrival order in the group (a relaxed add
-// taken when its stream ended).  Every CTA writes its partial rows and
+// taken by thread `ticket_tid` when its stream ended).  Every CTA writes its partial rows and
 // publishes them by a release store of the call's token into its flag; a
 // merging CTA waits (bounded by the plan's timeout) until every split of the
 // group has published -- the CTAs that arrived before it are running, and at
@@ -1164,13 +1444,13 @@ __device__ __forceinline__ void finish_item(const SplitParams &p, const Item &it
 template <int G, int NC, int NW>
 __device__ __forceinline__ void finish_item_spread(const SplitParams &p, const Item &it, const uint8_t *state,
                                                    uint8_t *merge_scratch, volatile int *misc, int tid,
-                                                   int ticket)
+                                                   int ticket, int ticket_tid)
 {
     combine_states<G, NC, NW>(p, it, state, tid, false);
     __syncthreads();
     const int total_splits = p.num_work / p.num_kv_heads;
     int *flags = p.flags + (int64_t)it.kvh * total_splits + it.prefix;
-    if (tid == 0) {
+    if (tid == ticket_tid) {
         if (ticket == it.splits - 1)   // every CTA of the group has taken its ticket
             cuda::atomic_ref<int, cuda::thread_scope_device>(
                 p.counters[(int64_t)it.b * p.num_kv_heads + it.kvh])
@@ -1251,12 +1531,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     if (!early_derive)
         griddep_wait();
 
-    float m_run = -INFINITY, l_part = 0.f, vscale = 1.f;
-    int v_exp = kNoExp;   // INT4: see consume_tile
-    float o_acc[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-        o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+    float vscale = 1.f;              // FP8: the head's V scale
+    Consumer<G, KV, DT> cs;          // consumer warps: set up by begin()
 
     if (warp == NC) {
         // ---------------------------------------------------------- producer
@@ -1478,13 +1754,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         const Item it = read_item(desc);
         if (it.state == kItemOk) {
             uint32_t qa[8][2];
-            float qk = p.q_scale *
-                       load_q<G, DT, true>(p.q + ((int64_t)it.b * p.num_qo_heads + kvh * G) * kHeadDim,
-                                           lane, qa);
+            float qk = p.q_scale * load_q<G, DT, true, kColumnForm<G, DT>>(
+                                       p.q + ((int64_t)it.b * p.num_qo_heads + kvh * G) * kHeadDim, lane, qa);
             if constexpr (DT == kKvFp8) {   // the head's dequantisation scales
                 qk *= __ldg(p.k_scale + kvh);
                 vscale = __ldg(p.v_scale + kvh);
             }
+            cs.begin(qk, lane);
             const uint32_t ring = smem_addr(smem);
             const int n_tiles = (it.t1 - it.t0 + kTile - 1) / kTile;
             for (int i = warp; i < n_tiles; i += NC) {
@@ -1495,8 +1771,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                         report(p.status, FD_ERR_TIMEOUT);
                     break;
                 }
-                consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc, v_exp);
+                cs.tile(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa, lane);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1530,17 +1805,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     // others' flags); the arrival ticket is taken now, so its round trip
     // overlaps the combine.  Measured (back to back, interleaved): 64k keys
     // 40.1 -> 39.7 us, FP8 26.1 -> 25.3 us, 128k FP8 43.9 -> 42.9 us.
+    // The producer warp's lane takes it: it has no consumer state to write,
+    // and a warp with the atomic in flight was measured to run its shuffles
+    // about 100 ns each (warp 0 taking it: 64k INT4 column form +4.5 us).
     const bool spread = G > 1 && p.fuse_merge && p.flags != nullptr && it.splits > 1;
+    constexpr int kTicketTid = NC * 32;
     int ticket = 0;
-    if (spread && tid == 0)
+    if (spread && tid == kTicketTid)
         ticket = atomicAdd(p.counters + (int64_t)it.b * p.num_kv_heads + it.kvh, 1);
-    if constexpr (DT == kKvInt4)
-        vscale = v_exp == kNoExp ? 1.f : pow2i(v_exp);
     if (warp < NC)
-        write_state<G, NC, DT>(smem, warp, lane, o_acc, m_run, l_part, vscale);
+        cs.template write<NC>(smem, warp, lane, vscale);
     __syncthreads();
     if (spread)
-        finish_item_spread<G, NC, NC + 1>(p, it, smem, smem, misc, tid, ticket);
+        finish_item_spread<G, NC, NC + 1>(p, it, smem, smem, misc, tid, ticket, kTicketTid);
     else
         finish_item<G, NC, NC + 1, 0>(p, it, smem, smem, misc, tid, [] {});
     // This CTA's outputs are written: a dependent grid may launch.
@@ -1778,16 +2055,12 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
         Item it = read_item(desc);
         while (ok && it.state == kItemOk) {
             const int slot = k % kDescSlots;
-            float m_run = -INFINITY, l_part = 0.f;
-            int v_exp = kNoExp;   // INT4: see consume_tile
-            float o_acc[16][4];
-#pragma unroll
-            for (int n = 0; n < 16; ++n)
-                o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
             uint32_t qa[8][2];
-            const float qk = p.q_scale * __int_as_float(it.ks) *
-                             load_q<G, DT, false>(reinterpret_cast<const uint16_t *>(qslots + slot * L::kQSlot),
-                                                  lane, qa);
+            Consumer<G, KV, DT> cs;
+            cs.begin(p.q_scale * __int_as_float(it.ks) *
+                         load_q<G, DT, false, kColumnForm<G, DT>>(
+                             reinterpret_cast<const uint16_t *>(qslots + slot * L::kQSlot), lane, qa),
+                     lane);
             const int n_tiles = (it.t1 - it.t0 + kTile - 1) / kTile;
             // this warp's tiles of the item: stream tiles g = warp (mod NC)
             const int first = it.gt0 + ((warp - it.gt0 % NC) + NC) % NC;
@@ -1801,8 +2074,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                     ok = false;
                     break;
                 }
-                consume_tile<KV, DT>(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa,
-                                     qk, lane, m_run, l_part, o_acc, v_exp);
+                cs.tile(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa, lane);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&bars[NS + s]));
@@ -1827,9 +2099,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, MIN_CTAS)
                     report(p.status, FD_ERR_TIMEOUT);
                 break;
             }
-            write_state<G, NC, DT>(states + sb * L::kStateBytes, warp, lane, o_acc, m_run, l_part,
-                                   DT == kKvInt4 ? (v_exp == kNoExp ? 1.f : pow2i(v_exp))
-                                                 : __int_as_float(it.vs));
+            cs.template write<NC>(states + sb * L::kStateBytes, warp, lane, __int_as_float(it.vs));
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&state_full[sb]));
@@ -1961,23 +2231,37 @@ constexpr int stages_for()
     return DT == kKvBf16 ? kNS : 2 * kNS;
 }
 
-// Consumer warps (and stages, two per warp) of the one-item kernel for INT4
-// K/V: its consumers are the bound (codes widened in registers), and a fifth
-// consumer warp still fits the register file at two CTAs per SM (12 warps x
-// 168 registers).  Measured: 64k step -2 %, 128k -4.5 %; FP8 was slower with 5.
+// Consumer warps (and stages, two per warp) for INT4 K/V, whose consumers
+// are the bound (codes widened in registers).  Row form (G = 8), one-item
+// kernel: a fifth consumer warp still fits the register file at two CTAs per
+// SM (12 warps x 168 registers; 64k step -2 %, 128k -4.5 %; FP8 was slower
+// with 5).  Column form (G <= 4, ~40 registers fewer): five in the one-item
+// kernel (six or seven were slower there: 64k 24.8 us with five, 26.9 with
+// six, 26.1 with seven) and six in the persistent kernel (ragged batch
+// 184.9 -> 180.9 us against four).
 constexpr int kNCInt4 = 5;
+#ifndef FD_SPLIT_INT4_COLUMN_WARPS
+#define FD_SPLIT_INT4_COLUMN_WARPS 5
+#endif
+#ifndef FD_SPLIT_INT4_COLUMN_PWARPS
+#define FD_SPLIT_INT4_COLUMN_PWARPS 6
+#endif
+constexpr int kNCInt4Cols = FD_SPLIT_INT4_COLUMN_WARPS;     // one-item kernel, column form
+constexpr int kNCInt4ColsP = FD_SPLIT_INT4_COLUMN_PWARPS;   // persistent kernel, column form
 
 // One wave of items: one item per CTA.  More: the persistent kernel on
 // num_ctas CTAs.
 template <int G, int KV, int DT>
 cudaError_t launch_g(const KvMaps &m, const SplitParams &p, int num_ctas, cudaStream_t stream)
 {
-    constexpr int NS = stages_for<DT>();
-    constexpr int NC1 = DT == kKvInt4 ? kNCInt4 : kNC;           // one-item kernel
-    constexpr int NS1 = DT == kKvInt4 ? 2 * kNCInt4 : NS;
+    constexpr bool cols = kColumnForm<G, DT>;
+    constexpr int NC1 = DT != kKvInt4 ? kNC : cols ? kNCInt4Cols : kNCInt4;   // one-item kernel
+    constexpr int NS1 = DT == kKvInt4 ? 2 * NC1 : stages_for<DT>();
+    constexpr int NCP = cols ? kNCInt4ColsP : kNC;                          // persistent kernel
+    constexpr int NS = DT == kKvInt4 ? 2 * NCP : stages_for<DT>();
     using SG = Stage<KV, DT>;
     using LS = SingleLayout<G, NC1, NS1, SG::kBytes>;
-    using LP = PersistentLayout<G, kNC, NS, SG::kBytes>;
+    using LP = PersistentLayout<G, NCP, NS, SG::kBytes>;
     static_assert(kMinCtas * (LS::kAlloc + 1024) <= 233472 && kMinCtas * (LP::kAlloc + 1024) <= 233472,
                   "the resident CTAs must fit in shared memory");
     if (num_ctas >= p.num_work) {   // one wave: one item (or, device-side plan, at most one) per CTA
@@ -1986,7 +2270,7 @@ cudaError_t launch_g(const KvMaps &m, const SplitParams &p, int num_ctas, cudaSt
                              LS::kWarps * 32, p.num_work, m, p, stream);
     }
     static bool configured[64] = {};
-    return launch_kernel(split_kv_persistent_kernel<G, kNC, NS, kMinCtas, KV, DT>, configured,
+    return launch_kernel(split_kv_persistent_kernel<G, NCP, NS, kMinCtas, KV, DT>, configured,
                          LP::kAlloc, LP::kWarps * 32, num_ctas, m, p, stream);
 }
 
