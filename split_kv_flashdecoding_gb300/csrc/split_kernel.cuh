@@ -1105,26 +1105,35 @@ struct RowConsumer {
     }
 };
 
-// The column form for INT4 K/V and G <= 4: S^T = K Q^T and O^T = V^T P^T, the
-// tile's keys (scores) and the head's dims (output) in the MMA's 16 rows and
-// the query heads in its 8 columns, so every MMA row carries data: half the
-// MMAs and half the output accumulators of the row form, whose padding rows
-// 8-15 carry nothing in Q K^T.  Column n < G is head n with the hi part of
-// its P V weights, column G + n the same head with the lo part (the f16
-// weights keep about 22 bits, as in the row form), columns >= 2G repeat
+// The column form for FP8 and INT4 K/V with G <= 4: S^T = K Q^T and
+// O^T = V^T P^T, the tile's keys (scores) and the head's dims (output) in the
+// MMA's 16 rows and the query heads in its 8 columns, so every MMA row carries
+// data: half the MMAs and half the output accumulators of the row form, whose
+// padding rows 8-15 carry nothing in Q K^T.  Column n < G is head n with the
+// hi part of its P V weights, column G + n the same head with the lo part (the
+// f16 weights keep about 22 bits, as in the row form), columns >= 2G repeat
 // heads and are dropped.  Q fills every column (load_q<..., COLS>), so a lo
 // column computes the same scores, maxima and sums as its hi column in its
 // own lanes and needs no exchange until write().
 //  Lane (g, t4) holds scores of keys g, g + 8, 16 + g, 24 + g for columns
 //  2t4 and 2t4 + 1 (m[e], l[e], qk[e]: column 2t4 + e).  P^T as the B operand
-//  is the transpose of the score fragments (movmatrix).  o[2c + jp] holds
-//  dims 32c + 4g + 2jp (c0, c1) and + 1 (c2, c3) for the lane's two columns.
-template <int G, int KV>
+//  is the transpose of the score fragments (movmatrix).  Output m-block n
+//  holds, for the lane's two columns, dims dim0(n, g) (c0, c1) and
+//  dim0(n, g) + 1 (c2, c3): INT4 n = 2c + jp -> 32c + 4g + 2jp, FP8 n = c ->
+//  16c + 2g (the orders ldmatrix.trans and the widenings give).
+template <int G, int KV, int DT>
 struct ColumnConsumer {
     static_assert(G == 1 || G == 2 || G == 4, "column form: two columns per head");
+    static_assert(DT == kKvFp8 || DT == kKvInt4, "column form: FP8 or INT4 K/V");
+    static constexpr bool kInt4 = DT == kKvInt4;
     float o[8][4];
     float m[2], l[2], qk[2], lo[2];
-    int v_exp;
+    int v_exp;   // INT4: see consume_tile
+
+    static __device__ __forceinline__ int dim0(int n, int g)
+    {
+        return kInt4 ? 32 * (n >> 1) + 4 * g + 2 * (n & 1) : 16 * n + 2 * g;
+    }
 
     __device__ __forceinline__ void begin(float qk_row, int lane)
     {
@@ -1145,35 +1154,65 @@ struct ColumnConsumer {
 
     __device__ __forceinline__ void tile(uint32_t st, int n_valid, const uint32_t (&qa)[8][2], int lane)
     {
-        using S = Stage<KV, kKvInt4>;
+        using S = Stage<KV, DT>;
         const int g = lane >> 2, lr = lane & 7, lm = lane >> 3;
 
+        // FP8: V rows past the last key zeroed, as in consume_tile
+        if constexpr (!kInt4) {
+            if (n_valid < kTile) {
+                constexpr int kChunks = S::kRowBytes / 16;
+                const uint32_t vt = st + S::kTensorBytes;
+                for (int idx = lane; idx < (kTile - n_valid) * kChunks; idx += 32)
+                    sts_zero16(vt + S::chunk_offset(n_valid + idx / kChunks, idx % kChunks));
+                fence_proxy_async_shared();
+                __syncwarp();
+            }
+        }
+
         // ---- S^T = K Q^T: m-block mb = keys 16 mb + g (rows g), 16 mb + 8 + g
-        // (rows g + 8).  ldmatrix gives lane (g, t4) the codes of dims
-        // 32c + 8t4 .. +7 of a key in word c; widened, k-step 2c + h takes
-        // dims + 2h (+4) at k 2t4 (+1) and + 2h + 1 (+4) at k 2t4 + 8 (+9), the
-        // order load_q puts Q in.
+        // (rows g + 8); ldmatrix gives lane (g, t4) word t4 of each 16-byte
+        // chunk of a key row, widened in the dim order load_q puts Q in.
         float s[2][4];
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {
             s[mb][0] = s[mb][1] = s[mb][2] = s[mb][3] = 0.f;
-            uint32_t k0[4], k1[4];
             const int r0 = 16 * mb + lr, r1 = r0 + 8;
-            ldsm_x4(st + r0 * 64 + ((lm ^ ((r0 >> 1) & 3)) << 4), k0);
-            ldsm_x4(st + r1 * 64 + ((lm ^ ((r1 >> 1) & 3)) << 4), k1);
+            if constexpr (kInt4) {
+                // chunk c = dims 32c .. +31; k-step 2c + h takes dims
+                // 32c + 8t4 + 2h (+4) at k 2t4 (+1) and + 2h + 1 (+4) at k 2t4 + 8 (+9)
+                uint32_t k0[4], k1[4];
+                ldsm_x4(st + r0 * 64 + ((lm ^ ((r0 >> 1) & 3)) << 4), k0);
+                ldsm_x4(st + r1 * 64 + ((lm ^ ((r1 >> 1) & 3)) << 4), k1);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t a[4], b[4];   // [j]: dims 32c + 8t4 + j and + 4 of keys 16mb + g, + 8
-                int4x8_to_f16x2x4(k0[c], a);
-                int4x8_to_f16x2x4(k1[c], b);
-                mma_f16(s[mb], a[0], b[0], a[1], b[1], qa[2 * c][0], qa[2 * c][1]);
-                mma_f16(s[mb], a[2], b[2], a[3], b[3], qa[2 * c + 1][0], qa[2 * c + 1][1]);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t a[4], b[4];   // [j]: dims 32c + 8t4 + j and + 4 of keys 16mb + g, + 8
+                    int4x8_to_f16x2x4(k0[c], a);
+                    int4x8_to_f16x2x4(k1[c], b);
+                    mma_f16(s[mb], a[0], b[0], a[1], b[1], qa[2 * c][0], qa[2 * c][1]);
+                    mma_f16(s[mb], a[2], b[2], a[3], b[3], qa[2 * c + 1][0], qa[2 * c + 1][1]);
+                }
+            } else {
+                // chunk c = dims 16c .. +15 = k-step c: dims 16c + 4t4 (+1) at
+                // k 2t4 (+1), 16c + 4t4 + 2 (+3) at k 2t4 + 8 (+9)
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                    uint32_t k0[4], k1[4];
+                    ldsm_x4(st + r0 * 128 + (((4 * hc + lm) ^ lr) << 4), k0);
+                    ldsm_x4(st + r1 * 128 + (((4 * hc + lm) ^ lr) << 4), k1);
+#pragma unroll
+                    for (int mc = 0; mc < 4; ++mc) {
+                        uint32_t a0, a1, a2, a3;
+                        e4m3x4_to_f16x2x2(k0[mc], a0, a2);
+                        e4m3x4_to_f16x2x2(k1[mc], a1, a3);
+                        mma_f16(s[mb], a0, a1, a2, a3, qa[4 * hc + mc][0], qa[4 * hc + mc][1]);
+                    }
+                }
             }
         }
 
         // ---- online softmax per column over the warp's 32 keys (the 8 lanes
-        // of a t4 hold them: reductions over g), with the K and V scales of
-        // the lane's 4 keys; the V exponent as in the row form (consume_tile)
+        // of a t4 hold them: reductions over g); INT4: the lane's 4 keys' K
+        // and V scales, and the V exponent as in the row form (consume_tile)
         const uint32_t ks_base = st + S::kKsOff, vs_base = st + S::kVsOff;
         float x[2][4], vs[2][2];
         float mt0 = -INFINITY, mt1 = -INFINITY, vmax = 0.f;
@@ -1183,21 +1222,24 @@ struct ColumnConsumer {
             for (int hf = 0; hf < 2; ++hf) {
                 const int key = 16 * mb + 8 * hf + g;
                 const bool ok = key < n_valid;
-                const float ksc = lds_f32(ks_base + 4 * key);
+                const float ksc = kInt4 ? lds_f32(ks_base + 4 * key) : 1.f;
                 const float v0 = ok ? s[mb][2 * hf] * ksc * qk[0] : -INFINITY;
                 const float v1 = ok ? s[mb][2 * hf + 1] * ksc * qk[1] : -INFINITY;
                 x[mb][2 * hf] = v0;
                 x[mb][2 * hf + 1] = v1;
                 mt0 = fmaxf(mt0, v0);
                 mt1 = fmaxf(mt1, v1);
-                vs[mb][hf] = ok ? lds_f32(vs_base + 4 * key) : 0.f;
-                vmax = fmaxf(vmax, fabsf(vs[mb][hf]));
+                if constexpr (kInt4) {
+                    vs[mb][hf] = ok ? lds_f32(vs_base + 4 * key) : 0.f;
+                    vmax = fmaxf(vmax, fabsf(vs[mb][hf]));
+                }
             }
 #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
             mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, sh));
             mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, sh));
-            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, sh));
+            if constexpr (kInt4)
+                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, sh));
         }
         const float m0 = fmaxf(m[0], mt0), m1 = fmaxf(m[1], mt1);
         float os0 = exp2f(m[0] - m0), os1 = exp2f(m[1] - m1);
@@ -1215,13 +1257,15 @@ struct ColumnConsumer {
             }
         l[0] = fmaf(l[0], os0, ps0);
         l[1] = fmaf(l[1], os1, ps1);
-        if (!(vmax <= 0.f)) {   // a nonzero, inf or NaN scale: vmax < 2^e
-            const int e = ((__float_as_int(vmax) >> 23) & 0xFF) - 126;
-            if (e > v_exp) {
-                const float f = pow2i(v_exp - e);   // 0 when v_exp is still kNoExp
-                os0 *= f;
-                os1 *= f;
-                v_exp = e;
+        if constexpr (kInt4) {
+            if (!(vmax <= 0.f)) {   // a nonzero, inf or NaN scale: vmax < 2^e
+                const int e = ((__float_as_int(vmax) >> 23) & 0xFF) - 126;
+                if (e > v_exp) {
+                    const float f = pow2i(v_exp - e);   // 0 when v_exp is still kNoExp
+                    os0 *= f;
+                    os1 *= f;
+                    v_exp = e;
+                }
             }
         }
         if (__any_sync(0xffffffffu, os0 != 1.f || os1 != 1.f)) {
@@ -1235,60 +1279,83 @@ struct ColumnConsumer {
         }
 
         // ---- P^T (B operand of k-step mb: keys 16 mb + 2t4 (+1) in b0,
-        // + 8 in b1, column g): the weights p * v_scale * 2^-v_exp as f16 (hi
-        // columns) or their remainder after f16 (lo columns), packed per key
-        // row and transposed
-        const float vinv = v_exp == kNoExp ? 1.f : pow2i(-v_exp);
+        // + 8 in b1, column g): the weights (INT4: p * v_scale * 2^-v_exp) as
+        // f16 (hi columns) or their remainder after f16 (lo columns), packed
+        // per key row and transposed
+        const float vinv = kInt4 && v_exp != kNoExp ? pow2i(-v_exp) : 1.f;
         uint32_t pt[2][2];
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const float w = vs[mb][hf] * vinv;
-                float p0 = x[mb][2 * hf] * w, p1 = x[mb][2 * hf + 1] * w;
+                float p0 = x[mb][2 * hf], p1 = x[mb][2 * hf + 1];
+                if constexpr (kInt4) {
+                    const float w = vs[mb][hf] * vinv;
+                    p0 *= w;
+                    p1 *= w;
+                }
                 p0 = fmaf(-lo[0], f16_round(p0), p0);
                 p1 = fmaf(-lo[1], f16_round(p1), p1);
                 pt[mb][hf] = movmatrix_trans(pack_f16(p0, p1));
             }
 
-        // ---- O^T += V^T P^T: k-step ks = keys 16 ks .. +15; m-block (c, jp)
-        // = dims 32c + 4g + 2jp (rows g) and + 1 (rows g + 8).  ldmatrix.trans
-        // gives lane (g, t4) dims 32c + 4g .. +3 of keys 2t4 and 2t4 + 1 in one
-        // word, widened to (key 2t4, key 2t4 + 1) pairs per dim.
+        // ---- O^T += V^T P^T: k-step ks = keys 16 ks .. +15.  ldmatrix.trans
+        // matrix lm = keys 16 ks + 8 (lm & 1) .. +7 of chunk 2 cp + (lm >> 1)
         const uint32_t vt = st + S::kTensorBytes;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
-            // matrix lm: keys 16 ks + 8 (lm & 1) .. +7, chunk 2 cp + (lm >> 1)
             const int r = 16 * ks + 8 * (lm & 1) + lr;
+            if constexpr (kInt4) {
+                // lane (g, t4): dims 32c + 4g .. +3 of keys 2t4, 2t4 + 1 in one
+                // word, widened to (key 2t4, key 2t4 + 1) pairs per dim;
+                // m-block 2c + jp = dims + 2jp (rows g), + 2jp + 1 (rows g + 8)
 #pragma unroll
-            for (int cp = 0; cp < 2; ++cp) {
-                uint32_t vb[4];
-                ldsm_x4_trans(vt + r * 64 + (((2 * cp + (lm >> 1)) ^ ((r >> 1) & 3)) << 4), vb);
+                for (int cp = 0; cp < 2; ++cp) {
+                    uint32_t vb[4];
+                    ldsm_x4_trans(vt + r * 64 + (((2 * cp + (lm >> 1)) ^ ((r >> 1) & 3)) << 4), vb);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {   // chunk c = 2 cp + h
-                    const int c = 2 * cp + h;
-                    uint32_t a[4], b[4];        // [j]: dim 32c + 4g + j of keys 2t4, 2t4 + 1 (+8 in b)
-                    int4x8_to_f16x2x4(vb[2 * h], a);
-                    int4x8_to_f16x2x4(vb[2 * h + 1], b);
+                    for (int h = 0; h < 2; ++h) {   // chunk c = 2 cp + h
+                        const int c = 2 * cp + h;
+                        uint32_t a[4], b[4];        // [j]: dim 32c + 4g + j of keys 2t4, 2t4 + 1 (+8 in b)
+                        int4x8_to_f16x2x4(vb[2 * h], a);
+                        int4x8_to_f16x2x4(vb[2 * h + 1], b);
 #pragma unroll
-                    for (int jp = 0; jp < 2; ++jp)
-                        mma_f16(o[2 * c + jp], a[2 * jp], a[2 * jp + 1], b[2 * jp], b[2 * jp + 1],
-                                pt[ks][0], pt[ks][1]);
+                        for (int jp = 0; jp < 2; ++jp)
+                            mma_f16(o[2 * c + jp], a[2 * jp], a[2 * jp + 1], b[2 * jp], b[2 * jp + 1],
+                                    pt[ks][0], pt[ks][1]);
+                    }
+                }
+            } else {
+                // lane (g, t4): dims 16c + 2g, + 1 of keys 2t4, 2t4 + 1,
+                // regrouped per dim; m-block c = dims 16c + 2g (rows g), + 1
+                // (rows g + 8)
+#pragma unroll
+                for (int cp = 0; cp < 4; ++cp) {
+                    uint32_t vb[4];
+                    ldsm_x4_trans(vt + r * 128 + (((2 * cp + (lm >> 1)) ^ lr) << 4), vb);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {   // chunk c = 2 cp + h
+                        uint32_t a0, a1, a2, a3;
+                        e4m3x4_to_f16x2x2(__byte_perm(vb[2 * h], 0u, 0x3120), a0, a1);
+                        e4m3x4_to_f16x2x2(__byte_perm(vb[2 * h + 1], 0u, 0x3120), a2, a3);
+                        mma_f16(o[2 * cp + h], a0, a1, a2, a3, pt[ks][0], pt[ks][1]);
+                    }
                 }
             }
         }
     }
 
     // O of head n = hi column n + lo column G + n (lane ^ G/2, or the lane's
-    // other column for G = 1), times 2^v_exp; the row sums summed over g.
+    // other column for G = 1), times the V scale (INT4: 2^v_exp; FP8: the
+    // head's); the row sums summed over g.
     template <int NC>
-    __device__ __forceinline__ void write(uint8_t *state, int warp, int lane, float) const
+    __device__ __forceinline__ void write(uint8_t *state, int warp, int lane, float fp8_vscale) const
     {
         float *comb_acc = reinterpret_cast<float *>(state);
         float *comb_m = comb_acc + NC * G * kHeadDim;
         float *comb_l = comb_m + NC * G;
         const int g = lane >> 2, t4 = lane & 3;
-        const float vscale = v_exp == kNoExp ? 1.f : pow2i(v_exp);
+        const float vscale = !kInt4 ? fp8_vscale : v_exp == kNoExp ? 1.f : pow2i(v_exp);
         float lt[2] = {l[0], l[1]};
 #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
@@ -1297,13 +1364,11 @@ struct ColumnConsumer {
         }
         if constexpr (G == 1) {
             if (t4 == 0) {
-                float *dst = comb_acc + warp * kHeadDim + 4 * g;
+                float *dst = comb_acc + warp * kHeadDim;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<float4 *>(dst + 32 * c) =
-                        make_float4((o[2 * c][0] + o[2 * c][1]) * vscale, (o[2 * c][2] + o[2 * c][3]) * vscale,
-                                    (o[2 * c + 1][0] + o[2 * c + 1][1]) * vscale,
-                                    (o[2 * c + 1][2] + o[2 * c + 1][3]) * vscale);
+                for (int n = 0; n < 8; ++n)
+                    *reinterpret_cast<float2 *>(dst + dim0(n, g)) =
+                        make_float2((o[n][0] + o[n][1]) * vscale, (o[n][2] + o[n][3]) * vscale);
                 if (g == 0) {
                     comb_m[warp] = m[0];
                     comb_l[warp] = lt[0];
@@ -1319,12 +1384,11 @@ struct ColumnConsumer {
             if (t4 < G / 2) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {   // head 2t4 + e
-                    float *dst = comb_acc + (warp * G + 2 * t4 + e) * kHeadDim + 4 * g;
+                    float *dst = comb_acc + (warp * G + 2 * t4 + e) * kHeadDim;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<float4 *>(dst + 32 * c) =
-                            make_float4(tot[2 * c][e] * vscale, tot[2 * c][2 + e] * vscale,
-                                        tot[2 * c + 1][e] * vscale, tot[2 * c + 1][2 + e] * vscale);
+                    for (int n = 0; n < 8; ++n)
+                        *reinterpret_cast<float2 *>(dst + dim0(n, g)) =
+                            make_float2(tot[n][e] * vscale, tot[n][2 + e] * vscale);
                     if (g == 0) {
                         comb_m[warp * G + 2 * t4 + e] = m[e];
                         comb_l[warp * G + 2 * t4 + e] = lt[e];
@@ -1335,11 +1399,11 @@ struct ColumnConsumer {
     }
 };
 
-// INT4 K/V with G <= 4 take the column form.
+// FP8 and INT4 K/V with G <= 4 take the column form.
 template <int G, int DT>
-constexpr bool kColumnForm = DT == kKvInt4 && G <= 4;
+constexpr bool kColumnForm = (DT == kKvFp8 || DT == kKvInt4) && G <= 4;
 template <int G, int KV, int DT>
-using Consumer = std::conditional_t<kColumnForm<G, DT>, ColumnConsumer<G, KV>, RowConsumer<G, KV, DT>>;
+using Consumer = std::conditional_t<kColumnForm<G, DT>, ColumnConsumer<G, KV, DT>, RowConsumer<G, KV, DT>>;
 
 // Combine the NC consumer states in `state` (NW warps, thread `tid` of
 // NW * 32) into the item's normalised partial rows, or, when `direct`, into
@@ -2223,14 +2287,6 @@ cudaError_t launch_kernel(Kernel kern, bool (&configured)[64], int smem_bytes, i
     return cudaLaunchKernelEx(&cfg, kern, m.k, m.v, p);
 }
 
-// Stages in the ring: FP8 and INT4 tiles are half the bytes or less, so the
-// ring holds twice as many (two per consumer warp).
-template <int DT>
-constexpr int stages_for()
-{
-    return DT == kKvBf16 ? kNS : 2 * kNS;
-}
-
 // Consumer warps (and stages, two per warp) for INT4 K/V, whose consumers
 // are the bound (codes widened in registers).  Row form (G = 8), one-item
 // kernel: a fifth consumer warp still fits the register file at two CTAs per
@@ -2248,6 +2304,17 @@ constexpr int kNCInt4 = 5;
 #endif
 constexpr int kNCInt4Cols = FD_SPLIT_INT4_COLUMN_WARPS;     // one-item kernel, column form
 constexpr int kNCInt4ColsP = FD_SPLIT_INT4_COLUMN_PWARPS;   // persistent kernel, column form
+// FP8, column form: six consumer warps in the one-item kernel (64k 23.4 us
+// with four, 23.3 with five, 22.9 with six), four in the persistent kernel
+// (ragged batch 164.7 us; five: 170.5; six do not fit two CTAs' shared memory).
+#ifndef FD_SPLIT_FP8_COLUMN_WARPS
+#define FD_SPLIT_FP8_COLUMN_WARPS 6
+#endif
+#ifndef FD_SPLIT_FP8_COLUMN_PWARPS
+#define FD_SPLIT_FP8_COLUMN_PWARPS 4
+#endif
+constexpr int kNCFp8Cols = FD_SPLIT_FP8_COLUMN_WARPS;
+constexpr int kNCFp8ColsP = FD_SPLIT_FP8_COLUMN_PWARPS;
 
 // One wave of items: one item per CTA.  More: the persistent kernel on
 // num_ctas CTAs.
@@ -2255,10 +2322,13 @@ template <int G, int KV, int DT>
 cudaError_t launch_g(const KvMaps &m, const SplitParams &p, int num_ctas, cudaStream_t stream)
 {
     constexpr bool cols = kColumnForm<G, DT>;
-    constexpr int NC1 = DT != kKvInt4 ? kNC : cols ? kNCInt4Cols : kNCInt4;   // one-item kernel
-    constexpr int NS1 = DT == kKvInt4 ? 2 * NC1 : stages_for<DT>();
-    constexpr int NCP = cols ? kNCInt4ColsP : kNC;                          // persistent kernel
-    constexpr int NS = DT == kKvInt4 ? 2 * NCP : stages_for<DT>();
+    // consumer warps of the one-item and the persistent kernel; FP8 and INT4
+    // tiles are half the bytes or less, so their rings hold two stages per
+    // consumer warp
+    constexpr int NC1 = DT == kKvInt4 ? (cols ? kNCInt4Cols : kNCInt4) : DT == kKvFp8 && cols ? kNCFp8Cols : kNC;
+    constexpr int NCP = DT == kKvInt4 && cols ? kNCInt4ColsP : DT == kKvFp8 && cols ? kNCFp8ColsP : kNC;
+    constexpr int NS1 = DT == kKvBf16 ? kNS : 2 * NC1;
+    constexpr int NS = DT == kKvBf16 ? kNS : 2 * NCP;
     using SG = Stage<KV, DT>;
     using LS = SingleLayout<G, NC1, NS1, SG::kBytes>;
     using LP = PersistentLayout<G, NCP, NS, SG::kBytes>;
