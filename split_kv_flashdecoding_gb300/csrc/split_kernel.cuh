@@ -125,20 +125,21 @@ enum Misc { kAbort, kIssued, kDescs, kLast, kFinalK, kMiscCount };
 // warps: request, its split prefix and count, split, key range [t0, t1)
 // relative to the request's first key, KV head, index of the item's first
 // tile in the CTA's stream of tiles, the head's K and V scales (FP8 K/V; float
-// bits), and a state: kItemOk, kItemBad (outside the plan: the CTA stops) or
-// kItemEnd (no further item; the previous one was the CTA's last).
-enum Desc { kDB, kDPrefix, kDSplits, kDS, kDT0, kDT1, kDKvh, kDGt0, kDState, kDKs, kDVs, kDescInts };
+// bits), the request's first key row or page-list entry, and a state:
+// kItemOk, kItemBad (outside the plan: the CTA stops) or kItemEnd (no further
+// item; the previous one was the CTA's last).
+enum Desc { kDB, kDPrefix, kDSplits, kDS, kDT0, kDT1, kDKvh, kDGt0, kDState, kDKs, kDVs, kDBase, kDescInts };
 enum ItemState { kItemBad = 0, kItemOk = 1, kItemEnd = 2 };
 constexpr int kDescSlots = 4;
 
 struct Item {
-    int32_t b, prefix, splits, s, t0, t1, kvh, gt0, state, ks, vs;
+    int32_t b, prefix, splits, s, t0, t1, kvh, gt0, state, ks, vs, base;
 };
 
 __device__ __forceinline__ Item read_item(const volatile int *d)
 {
     return Item{d[kDB], d[kDPrefix], d[kDSplits], d[kDS], d[kDT0], d[kDT1],
-                d[kDKvh], d[kDGt0], d[kDState], d[kDKs], d[kDVs]};
+                d[kDKvh], d[kDGt0], d[kDState], d[kDKs], d[kDVs], d[kDBase]};
 }
 
 // Shared memory of the one-item kernel: [stage ring | full[NS] empty[NS] |
@@ -816,6 +817,33 @@ struct TileSource {
         }
     }
 
+    // cp.async (INT4, every lane): the lane's share of the 16-byte chunks of
+    // a tile's rows ya.. (yb.. for the second 16 rows of a paged tile) in both
+    // tensors (rows past the end of K/V zero-filled) and the K and V scale of
+    // row `lane`, into the stage at shared address dst.
+    __device__ __forceinline__ void copy_direct(uint32_t dst, int kvh, int32_t ya, int32_t yb) const
+    {
+        constexpr int kChunks = SL::kRowBytes / 16;   // per key row
+        const int64_t row_stride = (int64_t)p.num_kv_heads * SL::kRowBytes;
+        const uint8_t *kb = p.k_data + kvh * SL::kRowBytes;
+        const uint8_t *vb = p.v_data + kvh * SL::kRowBytes;
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+            const int idx = lane + 32 * i, r = idx / kChunks, c = idx % kChunks;
+            const int32_t row = SL::kBoxRows == kTile || r < 16 ? ya + r : yb + (r - 16);
+            const bool in = row < p.kv_rows;
+            const int64_t off = (int64_t)(in ? row : 0) * row_stride + c * 16;
+            const uint32_t so = SL::chunk_offset(r, c);
+            cp_async_16(dst + so, kb + off, in ? 16 : 0, pol);
+            cp_async_16(dst + SL::kTensorBytes + so, vb + off, in ? 16 : 0, pol);
+        }
+        const int32_t row = SL::kBoxRows == kTile || lane < 16 ? ya + lane : yb + (lane - 16);
+        const bool in = row < p.kv_rows;
+        const int64_t si = (int64_t)kvh * p.kv_rows + (in ? row : 0);
+        cp_async_4(dst + SL::kKsOff + 4 * lane, p.k_scale + si, in ? 4 : 0);
+        cp_async_4(dst + SL::kVsOff + 4 * lane, p.v_scale + si, in ? 4 : 0);
+    }
+
     // Put stream tile g (KV head kvh) into stage g % NS.
     //  TMA (lane 0): per tensor and per box of rows -- bf16, one 3-D box of
     //    both 64-column halves; FP8, one 2-D box of the rows' 128 bytes.
@@ -828,25 +856,7 @@ struct TileSource {
         const uint32_t bar = smem_addr(&full[s]);
         const uint32_t dst = smem_addr(ring + s * SL::kBytes);
         if constexpr (SL::kDirect) {
-            constexpr int kChunks = SL::kRowBytes / 16;   // per key row
-            const int64_t row_stride = (int64_t)p.num_kv_heads * SL::kRowBytes;
-            const uint8_t *kb = p.k_data + kvh * SL::kRowBytes;
-            const uint8_t *vb = p.v_data + kvh * SL::kRowBytes;
-#pragma unroll
-            for (int i = 0; i < kChunks; ++i) {
-                const int idx = lane + 32 * i, r = idx / kChunks, c = idx % kChunks;
-                const int32_t row = SL::kBoxRows == kTile || r < 16 ? ya + r : yb + (r - 16);
-                const bool in = row < p.kv_rows;
-                const int64_t off = (int64_t)(in ? row : 0) * row_stride + c * 16;
-                const uint32_t so = SL::chunk_offset(r, c);
-                cp_async_16(dst + so, kb + off, in ? 16 : 0, pol);
-                cp_async_16(dst + SL::kTensorBytes + so, vb + off, in ? 16 : 0, pol);
-            }
-            const int32_t row = SL::kBoxRows == kTile || lane < 16 ? ya + lane : yb + (lane - 16);
-            const bool in = row < p.kv_rows;
-            const int64_t si = (int64_t)kvh * p.kv_rows + (in ? row : 0);
-            cp_async_4(dst + SL::kKsOff + 4 * lane, p.k_scale + si, in ? 4 : 0);
-            cp_async_4(dst + SL::kVsOff + 4 * lane, p.v_scale + si, in ? 4 : 0);
+            copy_direct(dst, kvh, ya, yb);
             cp_async_mbar_arrive(bar);
         } else {
             mbar_arrive_expect_tx(bar, SL::kBytes);
@@ -905,6 +915,7 @@ __device__ __forceinline__ void write_desc(volatile int *d, const SplitCoord &c,
     d[kDT1] = t1;
     d[kDKvh] = kvh;
     d[kDGt0] = gt0;
+    d[kDBase] = c.base;
     d[kDState] = state;
 }
 
@@ -1577,6 +1588,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
     using L = SingleLayout<G, NC, NS, SG::kBytes>;
     constexpr bool paged = KV != kKvRagged;
     constexpr bool warp_loop = paged || SG::kDirect;   // the whole producer warp runs the issue loop
+    // Ragged FP8 and INT4: each consumer warp refills its own stages (see the
+    // consumers); INT4 also makes its first copies itself.
+    constexpr bool self_fill = !paged && DT == kKvInt4;
+    constexpr bool self_refill = !paged && DT != kKvBf16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1689,7 +1704,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
         }
         __syncwarp();
         TileSource<NS, KV, DT> src(p, &tm_k, &tm_v, smem, bars, lane);
-        const int n_tiles = ok ? (t1 - t0 + kTile - 1) / kTile : 0;
+        const int n_tiles = ok && !self_fill ? (t1 - t0 + kTile - 1) / kTile : 0;
         const int first = min(NS, n_tiles);
         if (ok && (warp_loop || lane == 0)) {
             src.begin_item(t0, c.base, c.pages);
@@ -1705,112 +1720,37 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
             for (int s = 0; s < NS; ++s)
                 fills[s] = s < first ? 1 : 0;
         __syncthreads();   // the barriers are initialised
-        if (ok && (warp_loop || lane == 0)) {
-            if constexpr (!paged && DT != kKvBf16) {
-                // FP8 and INT4 (consumers bound by their arithmetic, at uneven
-                // speeds): refills out of order across the consumer warps.
-                // Stage s belongs to warp s % NC, whose tiles w, w + NC, ... are
-                // refilled in order, but a warp's stage is refilled as soon as
-                // that warp frees it, without waiting behind a slower warp's
-                // stage.  The empty barriers are probed without blocking; the
-                // idle time since the last refill is bounded by the plan's
-                // timeout.  Measured (64k keys): INT4 32.6 -> 31.6 us, FP8
-                // 25.6 -> 24.9 us; bf16 0.7 us slower than in order.
-                int nxt[NC];
-#pragma unroll
-                for (int w = 0; w < NC; ++w)
-                    nxt[w] = first + ((w - first % NC) % NC + NC) % NC;
-                int left = n_tiles - first;
-                uint64_t idle_since = 0;
-                while (left > 0) {
-                    bool progressed = false;
-#pragma unroll
-                    for (int w = 0; w < NC; ++w) {
-                        const int i = nxt[w];
-                        if (i >= n_tiles)
-                            continue;
-                        int go = 0;
-                        if (lane == 0)
-                            go = mbar_test(smem_addr(&bars[NS + i % NS]), ((i / NS) - 1) & 1);
-                        if constexpr (warp_loop)
-                            go = __shfl_sync(0xffffffffu, go, 0);
-                        if (!go)
-                            continue;
-                        int32_t ya = 0, yb = 0;
-                        src.tile_rows(i, ya, yb);
-                        if (SG::kDirect || lane == 0)
-                            src.issue(i, kvh, ya, yb);
-                        nxt[w] = i + NC;
-                        --left;
-                        progressed = true;
+        if (ok && (warp_loop || lane == 0) && !self_refill) {
+            // The producer refills in order (paged K/V: its cursor only moves
+            // forward; bf16 K/V: bound by HBM, every warp as fast as its data,
+            // in-order refills measured faster than out-of-order ones).
+            int issued = first;
+            for (int i = first; i < n_tiles; ++i) {
+                int32_t ya = 0, yb = 0;
+                src.tile_rows(i, ya, yb);
+                int go = 0;
+                if (lane == 0) {
+                    go = mbar_wait(smem_addr(&bars[NS + i % NS]), ((i / NS) - 1) & 1, p.timeout_ns);
+                    if (!go) {
+                        misc[kAbort] = 1;
+                        report(p.status, FD_ERR_TIMEOUT);
+                    } else if (misc[kAbort]) {
+                        go = 0;
                     }
-                    if (progressed) {
-                        idle_since = 0;
-                        continue;
-                    }
-                    int stop = 0;
-                    if (lane == 0) {
-                        // No stage free: sleep on the stage of the oldest
-                        // outstanding tile (the likeliest to free next) for at
-                        // most a short while, then probe all of them again.
-                        int oldest = nxt[0];
-#pragma unroll
-                        for (int w = 1; w < NC; ++w)
-                            oldest = min(oldest, nxt[w]);
-                        mbar_try_wait_for(smem_addr(&bars[NS + oldest % NS]), ((oldest / NS) - 1) & 1, 200);
-                        const uint64_t now = global_timer_ns();
-                        if (misc[kAbort]) {
-                            stop = 1;
-                        } else if (idle_since == 0) {
-                            idle_since = now;
-                        } else if ((int64_t)(now - idle_since) > p.timeout_ns) {
-                            misc[kAbort] = 1;
-                            report(p.status, FD_ERR_TIMEOUT);
-                            stop = 1;
-                        }
-                    }
-                    if constexpr (warp_loop)
-                        stop = __shfl_sync(0xffffffffu, stop, 0);
-                    if (stop)
-                        break;
-                }
-                if (lane == 0)
-                    for (int s = 0; s < NS; ++s) {
-                        const int last = nxt[s % NC] - 1;   // warp s % NC issued its tiles below nxt
-                        fills[s] = last >= s ? (last - s) / NS + 1 : 0;
-                    }
-            } else {
-                // In order: the paged cursor only moves forward; for bf16 K/V
-                // (bound by HBM, every warp as fast as its data) in-order
-                // refills measured faster than out-of-order ones.
-                int issued = first;
-                for (int i = first; i < n_tiles; ++i) {
-                    int32_t ya = 0, yb = 0;
-                    src.tile_rows(i, ya, yb);
-                    int go = 0;
-                    if (lane == 0) {
-                        go = mbar_wait(smem_addr(&bars[NS + i % NS]), ((i / NS) - 1) & 1, p.timeout_ns);
-                        if (!go) {
-                            misc[kAbort] = 1;
-                            report(p.status, FD_ERR_TIMEOUT);
-                        } else if (misc[kAbort]) {
-                            go = 0;
-                        }
-                        if (go && !SG::kDirect)
-                            src.issue(i, kvh, ya, yb);
-                    }
-                    if constexpr (warp_loop)
-                        go = __shfl_sync(0xffffffffu, go, 0);
-                    if (!go)
-                        break;
-                    if constexpr (SG::kDirect)
+                    if (go && !SG::kDirect)
                         src.issue(i, kvh, ya, yb);
-                    issued = i + 1;
                 }
-                if (lane == 0)
-                    for (int s = 0; s < NS; ++s)
-                        fills[s] = issued > s ? (issued - 1 - s) / NS + 1 : 0;
+                if constexpr (warp_loop)
+                    go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go)
+                    break;
+                if constexpr (SG::kDirect)
+                    src.issue(i, kvh, ya, yb);
+                issued = i + 1;
             }
+            if (lane == 0)
+                for (int s = 0; s < NS; ++s)
+                    fills[s] = issued > s ? (issued - 1 - s) / NS + 1 : 0;
         }
     } else {
         // ---------------------------------------------------------- consumers
@@ -1827,18 +1767,82 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
             cs.begin(qk, lane);
             const uint32_t ring = smem_addr(smem);
             const int n_tiles = (it.t1 - it.t0 + kTile - 1) / kTile;
-            for (int i = warp; i < n_tiles; i += NC) {
-                const int s = i % NS;
-                if (!mbar_wait(smem_addr(&bars[s]), (i / NS) & 1, p.timeout_ns)) {
-                    misc[kAbort] = 1;
-                    if (lane == 0)
-                        report(p.status, FD_ERR_TIMEOUT);
-                    break;
+            if constexpr (self_fill) {
+                // The warp's own pipeline over its stages warp + NC j (j < D):
+                // its k-th tile (warp + NC k) goes to stage (warp + NC k) % NS,
+                // one cp.async group per tile (an empty group past the last),
+                // so that waiting for all but the D - 1 newest groups waits for
+                // the tile about to be consumed.  No producer hop and no
+                // mbarrier between a freed stage and its refill, and nothing
+                // to time out: every wait is for this warp's own copies.
+                // Measured against out-of-order refills by the producer warp
+                // (back to back): 64k 24.82 -> 24.19 us, 128k 41.53 -> 41.00
+                // us, 2048 keys 6.51 -> 6.28 us; three or four stages per warp
+                // were slower.
+                constexpr int D = NS / NC;
+                static_assert(NS % NC == 0, "self-filled stages: D per consumer warp");
+                const TileSource<NS, KV, DT> fsrc(p, &tm_k, &tm_v, smem, bars, lane);
+                const int32_t y0 = it.base + it.t0;
+                auto fill = [&](int k) {
+                    const int i = warp + NC * k;
+                    if (i < n_tiles)
+                        fsrc.copy_direct(ring + (i % NS) * SG::kBytes, kvh, y0 + i * kTile, 0);
+                    cp_async_commit();
+                };
+#pragma unroll
+                for (int k = 0; k < D; ++k)
+                    fill(k);
+                for (int k = 0; warp + NC * k < n_tiles; ++k) {
+                    const int i = warp + NC * k;
+                    cp_async_wait_group<D - 1>();
+                    __syncwarp();   // every lane's copies of the tile have landed
+                    cs.tile(ring + (i % NS) * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa, lane);
+                    __syncwarp();   // every lane is done reading the stage
+                    fill(k + D);
                 }
-                cs.tile(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa, lane);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_addr(&bars[NS + s]));
+                cp_async_wait_group<0>();
+            } else {
+                const TileSource<NS, KV, DT> rsrc(p, &tm_k, &tm_v, smem, bars, lane);
+                int i = warp;
+                for (; i < n_tiles; i += NC) {
+                    const int s = i % NS;
+                    if (!mbar_wait(smem_addr(&bars[s]), (i / NS) & 1, p.timeout_ns)) {
+                        misc[kAbort] = 1;
+                        if (lane == 0)
+                            report(p.status, FD_ERR_TIMEOUT);
+                        break;
+                    }
+                    cs.tile(ring + s * SG::kBytes, min(kTile, it.t1 - (it.t0 + i * kTile)), qa, lane);
+                    __syncwarp();
+                    if constexpr (self_refill) {
+                        // FP8: lane 0 refills the stage it just freed with the
+                        // warp's tile after next (the producer issued the first
+                        // two); the proxy fence orders the warp's reads of the
+                        // stage before the TMA's writes.  Measured against
+                        // out-of-order refills by the producer warp (64k keys,
+                        // back to back): 22.85 -> 22.41 us, 128k 41.25 -> 40.40
+                        // us, 2048 keys 6.45 -> 6.31 us.
+                        if (lane == 0 && i + NS < n_tiles) {
+                            fence_proxy_async_shared();
+                            rsrc.issue(i + NS, kvh, it.base + it.t0 + (i + NS) * kTile, 0);
+                        }
+                    } else if (lane == 0) {
+                        mbar_arrive(smem_addr(&bars[NS + s]));
+                    }
+                }
+                if constexpr (self_refill) {
+                    // copies issued into the warp's two stages, for the drain
+                    // after an error: its first min(mine, done + 2) tiles,
+                    // done = the tiles it consumed (tile i stopped the loop)
+                    static_assert(NS == 2 * NC, "self-refilled stages: two per consumer warp");
+                    if (lane == 0) {
+                        const int mine = n_tiles > warp ? (n_tiles - warp + NC - 1) / NC : 0;
+                        const int done = (i - warp) / NC;
+                        const int issued = min(mine, done + 2);
+                        fills[warp] = (issued + 1) / 2;
+                        fills[warp + NC] = issued / 2;
+                    }
+                }
             }
         }
     }
@@ -2304,11 +2308,12 @@ constexpr int kNCInt4 = 5;
 #endif
 constexpr int kNCInt4Cols = FD_SPLIT_INT4_COLUMN_WARPS;     // one-item kernel, column form
 constexpr int kNCInt4ColsP = FD_SPLIT_INT4_COLUMN_PWARPS;   // persistent kernel, column form
-// FP8, column form: six consumer warps in the one-item kernel (64k 23.4 us
-// with four, 23.3 with five, 22.9 with six), four in the persistent kernel
-// (ragged batch 164.7 us; five: 170.5; six do not fit two CTAs' shared memory).
+// FP8, column form: four consumer warps in the one-item kernel (with the
+// consumers refilling their own stages: 64k 22.41 us with four, 22.38 with
+// five, but 128k 40.40 against 41.27), four in the persistent kernel (ragged
+// batch 164.7 us; five: 170.5; six do not fit two CTAs' shared memory).
 #ifndef FD_SPLIT_FP8_COLUMN_WARPS
-#define FD_SPLIT_FP8_COLUMN_WARPS 6
+#define FD_SPLIT_FP8_COLUMN_WARPS 4
 #endif
 #ifndef FD_SPLIT_FP8_COLUMN_PWARPS
 #define FD_SPLIT_FP8_COLUMN_PWARPS 4
