@@ -10,9 +10,11 @@
 // widening of the codes is the only dequantisation step on the operands, and
 // it is exact (one lop3 and one f16 subtract or multiply-add per pair of codes;
 // with the bf16 widening it replaced, which needed a shift per pair, the 64k
-// step took 31.7 us instead of 26.8).  The stages are filled by the producer warp's 16-byte cp.async
-// copies rather than TMA boxes (64-byte rows and 4-byte scales: measured
-// faster on multi-wave plans, equal on one wave).
+// step took 31.7 us instead of 26.8).  The stages are filled by 16-byte
+// cp.async copies rather than TMA boxes (64-byte rows and 4-byte scales:
+// measured faster on multi-wave plans, equal on one wave), made by the
+// consumer warps themselves on ragged one-item calls and by the producer warp
+// otherwise.
 #include "split_kernel.cuh"
 
 namespace fd {
