@@ -1831,16 +1831,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, MIN_CTAS)
                     }
                 }
                 if constexpr (self_refill) {
-                    // copies issued into the warp's two stages, for the drain
-                    // after an error: its first min(mine, done + 2) tiles,
-                    // done = the tiles it consumed (tile i stopped the loop)
-                    static_assert(NS == 2 * NC, "self-refilled stages: two per consumer warp");
+                    // copies issued into the warp's D stages, for the drain
+                    // after an error: its first min(mine, done + D) tiles,
+                    // done = the tiles it consumed (tile i stopped the loop);
+                    // its k-th tile went to stage warp + NC (k mod D)
+                    constexpr int D = NS / NC;
+                    static_assert(NS % NC == 0, "self-refilled stages: D per consumer warp");
                     if (lane == 0) {
                         const int mine = n_tiles > warp ? (n_tiles - warp + NC - 1) / NC : 0;
                         const int done = (i - warp) / NC;
-                        const int issued = min(mine, done + 2);
-                        fills[warp] = (issued + 1) / 2;
-                        fills[warp + NC] = issued / 2;
+                        const int issued = min(mine, done + D);
+#pragma unroll
+                        for (int j = 0; j < D; ++j)
+                            fills[warp + NC * j] = issued > j ? (issued - 1 - j) / D + 1 : 0;
                     }
                 }
             }

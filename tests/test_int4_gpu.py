@@ -33,7 +33,13 @@ CASES = [
     ("many_splits", 1, 32, 8, [5000]),          # one wave
     ("ragged_many", 6, 16, 2, [3000, 0, 17, 900, 4100, 1]),
     ("odd_offsets", 4, 8, 1, [5, 33, 63, 2049]),  # scale rows start at every offset mod 4
-    ("multi_wave_g8", 2, 64, 8, [9000, 2500]),  # more items than one wave: persistent kernel
+    ("two_requests_g8", 2, 64, 8, [9000, 2500]),  # one wave on 152 SMs (296 items)
+    # more items than one wave (600 on 152 SMs): the persistent kernel, in the
+    # row form (G = 8) and the column form (G <= 4: keys and dims in the MMA rows)
+    ("multi_wave_g8", 3, 64, 8, [16000, 16000, 3000]),
+    ("multi_wave_g4", 3, 32, 8, [16000, 16000, 3000]),
+    ("multi_wave_g2", 3, 16, 8, [16000, 16001, 2999]),
+    ("multi_wave_g1", 3, 8, 8, [16001, 15999, 3000]),
 ]
 
 KINDS = {"quantised": lambda inp: to_int4(inp), "random": lambda inp: random_int4(inp, seed=21)}
