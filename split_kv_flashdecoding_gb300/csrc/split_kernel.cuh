@@ -173,7 +173,9 @@ struct PersistentLayout {
     static constexpr int kWarps = NC + 2;
     static constexpr int kQBytes = G * kHeadDim * 2;                    // the item's G query rows
     static constexpr int kQSlot = (kQBytes + 127) / 128 * 128;
-    static constexpr int kStateBytes = NC * G * (kHeadDim + 2) * 4;     // [NC][G][128] acc, m, l
+    // [NC][G][128] acc, then m, l; rounded up so that the second buffer's
+    // float4 rows stay 16-byte aligned for any NC and G
+    static constexpr int kStateBytes = (NC * G * (kHeadDim + 2) * 4 + 127) / 128 * 128;
     static_assert(kWarps * G * (kHeadDim + 2) * 4 <= NS * SB,
                   "the last item's merge works over the drained ring");
     static constexpr int kOffQ = NS * SB;
@@ -2298,16 +2300,18 @@ cudaError_t launch_kernel(Kernel kern, bool (&configured)[64], int smem_bytes, i
 // are the bound (codes widened in registers).  Row form (G = 8), one-item
 // kernel: a fifth consumer warp still fits the register file at two CTAs per
 // SM (12 warps x 168 registers; 64k step -2 %, 128k -4.5 %; FP8 was slower
-// with 5).  Column form (G <= 4, ~40 registers fewer): five in the one-item
-// kernel (six or seven were slower there: 64k 24.8 us with five, 26.9 with
-// six, 26.1 with seven) and six in the persistent kernel (ragged batch
-// 184.9 -> 180.9 us against four).
+// with 5).  Column form (G <= 4, ~40 registers fewer), with the consumers
+// filling their own stages: four in the one-item kernel (64k 22.0 us with
+// four, 24.2 with five, 26.0 with three, 34.8 with two; 128k 35.9 against
+// 41.1 with five; three stages per warp were slower) and three in the
+// persistent kernel (ragged batch 168.4 us; four 185.4, six 182.7, two 221.3):
+// the consumer warps then spread evenly over the SM's four schedulers.
 constexpr int kNCInt4 = 5;
 #ifndef FD_SPLIT_INT4_COLUMN_WARPS
-#define FD_SPLIT_INT4_COLUMN_WARPS 5
+#define FD_SPLIT_INT4_COLUMN_WARPS 4
 #endif
 #ifndef FD_SPLIT_INT4_COLUMN_PWARPS
-#define FD_SPLIT_INT4_COLUMN_PWARPS 6
+#define FD_SPLIT_INT4_COLUMN_PWARPS 3
 #endif
 constexpr int kNCInt4Cols = FD_SPLIT_INT4_COLUMN_WARPS;     // one-item kernel, column form
 constexpr int kNCInt4ColsP = FD_SPLIT_INT4_COLUMN_PWARPS;   // persistent kernel, column form
