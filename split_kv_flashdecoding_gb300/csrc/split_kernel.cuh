@@ -76,9 +76,10 @@ enum KvType { kKvBf16 = 0, kKvFp8 = 1, kKvInt4 = 2 };
 //    lands 16 rows further.
 //  INT4: a tensor is [32 rows][64 bytes] (128 four-bit values), 16-byte chunks
 //    XOR-swizzled by (r / 2) % 4, then the rows' K scales and V scales (fp32,
-//    32 each).  INT4 stages are filled by the producer lanes' cp.async copies
-//    (kDirect): with 64-byte rows and per-row scales, TMA boxes cost more
-//    producer and copy-engine time per byte than the copies do.
+//    32 each).  INT4 stages are filled by 16-byte cp.async copies (kDirect;
+//    a consumer warp's own lanes on ragged one-item calls, the producer warp's
+//    otherwise): with 64-byte rows and per-row scales, TMA boxes cost more
+//    copy-engine time per byte than the copies do.
 template <int KV, int DT>
 struct Stage {
     static constexpr bool kFp8 = DT == kKvFp8;
