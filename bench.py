@@ -588,6 +588,10 @@ def workload_summary(case, m, world, peak) -> dict:
         "algorithmic_bytes_per_step": nb["step"],
         "total_tokens": case["T"], "chunk": info.chunk, "splits": info.total_splits,
         "ctas": info.num_work, "kernel": case["kernel"],
+        # a CUDA-graph replay runs step_calls decode steps: the flushed figures
+        # are one replay after one flush, divided by step_calls (only its first
+        # step starts from the flushed L2)
+        "flushed_steps_per_measure": case["step_calls"],
     }
 
 
